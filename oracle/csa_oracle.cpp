@@ -1,0 +1,338 @@
+// csa_oracle.cpp -- plain fp64 CPU definition of the CSA/HCA KV-compressor
+// gated-softmax pooling over THD-packed ragged sequences, forward and backward.
+//
+// TEST INFRASTRUCTURE. Only the test suite, the smoke check and the bench's CPU
+// baseline may load or call this code. It shares nothing with the CUDA library:
+// no headers, no helpers, no tables. It is written to be checked by eye against
+// the definition, not to be fast: plain nested loops over segments, blocks,
+// columns and window positions, all arithmetic in double.
+//
+// Sources (cited by page title and section):
+//  * "Megatron-LM PR #5984", commit "CSA: add fused Compressor forward+backward
+//    CuTe-DSL kernels": one fused region per direction over THD packs. It gathers
+//    each block's window, adds the positional embedding (ape) to the scores, applies
+//    the overlapping-window transform, takes a float32 softmax over the window
+//    positions, sums kv weighted by that softmax and casts the sum to bf16.
+//  * same page, commit "fold dKV/dScore zero-init into the backward kernel": the
+//    backward writes every dKV/dScore position. Slots that no window reads hold
+//    exact zeros: at coff=2 the first-half columns of each segment's last block,
+//    each segment's tail tokens (seqlen mod ratio), every token of a segment
+//    shorter than ratio, and every row past cu_seqlens[S]. dAPE is a sum over
+//    blocks.
+//  * same page, commit "widen the validated envelope to coff in {1, 2}": at coff=1
+//    a block's window is just its own ratio tokens and every position is valid.
+//  * "cudnn-frontend PR #710" (ratio=2): position-in-block indexing, the masking of
+//    the first block's previous half, the tails and the short segments are all
+//    defined for any ratio >= 1.
+// Column/half assignment at coff=2: the previous block's tokens contribute their
+// columns [0,d) and the block's own tokens their columns [d,2d), each with the ape
+// row of the token's position inside its own block and the same ape column. This
+// is the plainest reading the first-half zero class supports: the last block's
+// own first-half columns are unread because there is no following block.
+//
+// Readings where the pages are silent:
+//  * The bf16 cast's backward is the identity: gradients use the unrounded output.
+//  * Masked (first block, coff=2) positions take no part in the softmax (weight 0).
+//  * Rows outside [cu_seqlens[0], cu_seqlens[S]) get zero gradients.
+//  * Unconsumed slots are +0.0 (bit pattern 0x0000).
+//  * All roundings to bf16 and to fp32 are round-to-nearest-even.
+//
+// Parity pins (tests/test_oracle_pins.py): brute-force predicate evaluator on tiny
+// packs, closed form for total_comp, uniform-score and shift invariants, softmax
+// Jacobian identities, the ratio=1 identity, central finite differences, and a
+// hand-derived golden pack (tests/golden/).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+namespace {
+
+double bf16_bits_to_double(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+// Round a double to the nearest bf16 (8 significant bits, fp32 exponent range,
+// subnormals down to 2^-133), ties to even, in one step (no detour via fp32).
+uint16_t double_to_bf16_bits(double x) {
+  if (std::isnan(x)) return 0x7FC0;
+  const bool neg = std::signbit(x);
+  if (x == 0.0) return neg ? 0x8000 : 0x0000;
+  if (std::isinf(x)) return neg ? 0xFF80 : 0x7F80;
+  int e = 0;
+  std::frexp(x, &e);                         // |x| in [2^(e-1), 2^e)
+  int q = e - 8;                             // spacing of bf16 numbers in that binade
+  if (q < -133) q = -133;                    // subnormal spacing
+  const double y = std::ldexp(x, -q);        // exact: power-of-two scaling
+  const double r = std::nearbyint(y);        // round half to even (default mode)
+  const double v = std::ldexp(r, q);
+  if (std::fabs(v) >= std::ldexp(1.0, 128)) return neg ? 0xFF80 : 0x7F80;
+  const float f = static_cast<float>(v);     // exact: v has <= 8 significant bits
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// Error codes shared by every entry point of the oracle.
+enum { ORACLE_OK = 0, ORACLE_BAD_ARGS = 1, ORACLE_BAD_CU = 2, ORACLE_OUT_ROWS = 3,
+       ORACLE_DOUBLE_WRITE = 4 };
+
+int check_args(const int32_t* cu, int S, int ratio, int coff, int d, int64_t capacity) {
+  if (cu == nullptr || S < 0 || ratio < 1 || (coff != 1 && coff != 2) || d < 1 ||
+      capacity < 0)
+    return ORACLE_BAD_ARGS;
+  if (cu[0] < 0) return ORACLE_BAD_CU;
+  for (int s = 0; s < S; ++s)
+    if (cu[s + 1] < cu[s]) return ORACLE_BAD_CU;
+  if (static_cast<int64_t>(cu[S]) > capacity) return ORACLE_BAD_CU;
+  return ORACLE_OK;
+}
+
+int64_t count_blocks(const int32_t* cu, int S, int ratio) {
+  int64_t total = 0;
+  for (int s = 0; s < S; ++s) total += (cu[s + 1] - cu[s]) / ratio;
+  return total;
+}
+
+// One valid position of a pooling window: the token row and column it reads in
+// kv/score (and writes in dKV/dScore), and the flat index of its ape element.
+struct WindowPos {
+  int64_t token;
+  int64_t col;
+  int64_t ape_index;
+};
+
+// Window of block b (0-based) of the segment starting at token c, for output
+// column j < d. coff=1: the block's own ratio tokens at column j, ape row = the
+// position inside the block. coff=2: positions 0..ratio-1 are the previous block's
+// tokens at column j (absent for the first block), positions ratio..2*ratio-1 are
+// the block's own tokens at column d+j; ape row = the token's position inside its
+// own block, ape column = the column read.
+void window_of(int64_t c, int64_t b, int ratio, int coff, int d, int64_t j,
+               std::vector<WindowPos>& win) {
+  const int64_t C = static_cast<int64_t>(coff) * d;
+  win.clear();
+  if (coff == 1) {
+    for (int w = 0; w < ratio; ++w) {
+      const int64_t t = c + b * ratio + w;
+      win.push_back({t, j, static_cast<int64_t>(w) * C + j});
+    }
+    return;
+  }
+  if (b >= 1) {
+    for (int w = 0; w < ratio; ++w) {
+      const int64_t t = c + (b - 1) * ratio + w;
+      win.push_back({t, j, static_cast<int64_t>(w) * C + j});
+    }
+  }
+  for (int w = 0; w < ratio; ++w) {
+    const int64_t t = c + b * ratio + w;
+    win.push_back({t, d + j, static_cast<int64_t>(w) * C + d + j});
+  }
+}
+
+// Softmax statistics of one window, in double.
+struct WindowStats {
+  std::vector<double> x;  // score + ape
+  std::vector<double> v;  // kv
+  std::vector<double> p;  // softmax weights
+  double m = 0.0;         // max of x
+  double o = 0.0;         // sum_w p_w v_w (unrounded output)
+};
+
+void window_stats(const uint16_t* kv, const uint16_t* score, const float* ape, int64_t C,
+                  const std::vector<WindowPos>& win, WindowStats& st) {
+  const size_t n = win.size();
+  st.x.resize(n);
+  st.v.resize(n);
+  st.p.resize(n);
+  for (size_t i = 0; i < n; ++i) {
+    const int64_t flat = win[i].token * C + win[i].col;
+    st.x[i] = bf16_bits_to_double(score[flat]) + static_cast<double>(ape[win[i].ape_index]);
+    st.v[i] = bf16_bits_to_double(kv[flat]);
+  }
+  st.m = st.x[0];
+  for (size_t i = 1; i < n; ++i)
+    if (st.x[i] > st.m) st.m = st.x[i];
+  double z = 0.0;
+  for (size_t i = 0; i < n; ++i) {
+    st.p[i] = std::exp(st.x[i] - st.m);
+    z += st.p[i];
+  }
+  for (size_t i = 0; i < n; ++i) st.p[i] /= z;
+  st.o = 0.0;
+  for (size_t i = 0; i < n; ++i) st.o += st.p[i] * st.v[i];
+}
+
+// First-order size of the rounding error an fp32 evaluation of the same window
+// can make in the output, in units of the fp32 unit roundoff: the summands'
+// magnitudes plus the spread of kv around the output weighted by how far each
+// weight's exponent argument is from zero (the absolute error of an fp32
+// exponent argument is proportional to |x| + |m|).
+double output_error_mass(const WindowStats& st) {
+  double a = 0.0;
+  for (size_t i = 0; i < st.p.size(); ++i)
+    a += st.p[i] * (std::fabs(st.v[i]) +
+                    std::fabs(st.v[i] - st.o) * (1.0 + std::fabs(st.x[i]) + std::fabs(st.m)));
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+// total_comp = sum over segments of floor(seqlen / ratio); -1 on bad arguments.
+int64_t csa_oracle_total_comp(const int32_t* cu_seqlens, int S, int ratio) {
+  if (cu_seqlens == nullptr || S < 0 || ratio < 1) return -1;
+  for (int s = 0; s < S; ++s)
+    if (cu_seqlens[s + 1] < cu_seqlens[s]) return -1;
+  return count_blocks(cu_seqlens, S, ratio);
+}
+
+// Per output row o < out_rows: {segment, block inside segment, first token of the
+// block}; rows at or past total_comp get {-1, -1, -1}.
+int csa_oracle_map_blocks(const int32_t* cu_seqlens, int S, int ratio, int64_t out_rows,
+                          int32_t* seg_blk_base) {
+  if (cu_seqlens == nullptr || S < 0 || ratio < 1 || out_rows < 0 ||
+      (out_rows > 0 && seg_blk_base == nullptr))
+    return ORACLE_BAD_ARGS;
+  for (int64_t i = 0; i < out_rows * 3; ++i) seg_blk_base[i] = -1;
+  int64_t o = 0;
+  for (int s = 0; s < S; ++s) {
+    const int64_t n = (cu_seqlens[s + 1] - cu_seqlens[s]) / ratio;
+    for (int64_t b = 0; b < n; ++b, ++o) {
+      if (o >= out_rows) return ORACLE_OUT_ROWS;
+      seg_blk_base[o * 3 + 0] = s;
+      seg_blk_base[o * 3 + 1] = static_cast<int32_t>(b);
+      seg_blk_base[o * 3 + 2] = static_cast<int32_t>(cu_seqlens[s] + b * ratio);
+    }
+  }
+  return ORACLE_OK;
+}
+
+// Forward. kv, score: bf16 bit patterns [capacity, coff*d]; ape: fp32 [ratio, coff*d];
+// out_bf16: [out_rows, d] (rows past total_comp are left untouched).
+// Optional (may be NULL): out_f64 (unrounded outputs), out_err (error mass, see
+// output_error_mass).
+int csa_oracle_fwd(const uint16_t* kv, const uint16_t* score, const float* ape,
+                   const int32_t* cu_seqlens, int S, int ratio, int coff, int d,
+                   int64_t capacity, int64_t out_rows, uint16_t* out_bf16, double* out_f64,
+                   double* out_err) {
+  int rc = check_args(cu_seqlens, S, ratio, coff, d, capacity);
+  if (rc != ORACLE_OK) return rc;
+  if (kv == nullptr || score == nullptr || ape == nullptr || out_bf16 == nullptr)
+    return ORACLE_BAD_ARGS;
+  if (count_blocks(cu_seqlens, S, ratio) > out_rows) return ORACLE_OUT_ROWS;
+  const int64_t C = static_cast<int64_t>(coff) * d;
+  std::vector<WindowPos> win;
+  WindowStats st;
+  int64_t o = 0;
+  for (int s = 0; s < S; ++s) {
+    const int64_t c = cu_seqlens[s];
+    const int64_t n = (cu_seqlens[s + 1] - cu_seqlens[s]) / ratio;
+    for (int64_t b = 0; b < n; ++b, ++o) {
+      for (int64_t j = 0; j < d; ++j) {
+        window_of(c, b, ratio, coff, d, j, win);
+        window_stats(kv, score, ape, C, win, st);
+        out_bf16[o * d + j] = double_to_bf16_bits(st.o);
+        if (out_f64 != nullptr) out_f64[o * d + j] = st.o;
+        if (out_err != nullptr) out_err[o * d + j] = output_error_mass(st);
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+// Backward. dout: bf16 bits [out_rows, d]. Writes every element of dkv_bf16 and
+// dscore_bf16 ([capacity, coff*d]) and dape_f64 ([ratio, coff*d], the sum over all
+// blocks, overwritten). Optional (may be NULL): dkv_f64/dscore_f64 (unrounded),
+// dape_f32 (dape rounded to fp32), owners (int32 [capacity, coff*d]: how many
+// window positions read the slot; must be 0 or 1), dscore_err and dape_err (first-
+// order fp32 error masses in units of the fp32 unit roundoff), dape_abs (sum of
+// the absolute values of the terms of each dAPE entry).
+int csa_oracle_bwd(const uint16_t* kv, const uint16_t* score, const float* ape,
+                   const int32_t* cu_seqlens, const uint16_t* dout, int S, int ratio, int coff,
+                   int d, int64_t capacity, int64_t out_rows, uint16_t* dkv_bf16,
+                   uint16_t* dscore_bf16, double* dape_f64, double* dkv_f64, double* dscore_f64,
+                   float* dape_f32, int32_t* owners, double* dscore_err, double* dape_err,
+                   double* dape_abs) {
+  int rc = check_args(cu_seqlens, S, ratio, coff, d, capacity);
+  if (rc != ORACLE_OK) return rc;
+  if (kv == nullptr || score == nullptr || ape == nullptr || dkv_bf16 == nullptr ||
+      dscore_bf16 == nullptr || dape_f64 == nullptr)
+    return ORACLE_BAD_ARGS;
+  const int64_t total = count_blocks(cu_seqlens, S, ratio);
+  if (total > out_rows) return ORACLE_OUT_ROWS;
+  if (total > 0 && dout == nullptr) return ORACLE_BAD_ARGS;
+  const int64_t C = static_cast<int64_t>(coff) * d;
+  const int64_t slots = capacity * C;
+
+  // Every slot starts as an exact +0; consumed slots are overwritten below.
+  std::vector<double> gkv(static_cast<size_t>(slots), 0.0);
+  std::vector<double> gsc(static_cast<size_t>(slots), 0.0);
+  std::vector<double> gsc_err(dscore_err != nullptr ? static_cast<size_t>(slots) : 0, 0.0);
+  std::vector<int32_t> count(static_cast<size_t>(slots), 0);
+  for (int64_t i = 0; i < static_cast<int64_t>(ratio) * C; ++i) {
+    dape_f64[i] = 0.0;
+    if (dape_err != nullptr) dape_err[i] = 0.0;
+    if (dape_abs != nullptr) dape_abs[i] = 0.0;
+  }
+
+  std::vector<WindowPos> win;
+  WindowStats st;
+  int64_t o = 0;
+  for (int s = 0; s < S; ++s) {
+    const int64_t c = cu_seqlens[s];
+    const int64_t n = (cu_seqlens[s + 1] - cu_seqlens[s]) / ratio;
+    for (int64_t b = 0; b < n; ++b, ++o) {
+      for (int64_t j = 0; j < d; ++j) {
+        window_of(c, b, ratio, coff, d, j, win);
+        window_stats(kv, score, ape, C, win, st);
+        const double g = bf16_bits_to_double(dout[o * d + j]);
+        const double oerr = output_error_mass(st);
+        for (size_t i = 0; i < win.size(); ++i) {
+          const int64_t flat = win[i].token * C + win[i].col;
+          // d out / d kv_w = p_w ; d out / d x_w = p_w (kv_w - out)  (softmax Jacobian)
+          const double dk = st.p[i] * g;
+          const double ds = st.p[i] * g * (st.v[i] - st.o);
+          gkv[flat] = dk;
+          gsc[flat] = ds;
+          count[flat] += 1;
+          dape_f64[win[i].ape_index] += ds;
+          const double err = std::fabs(st.p[i] * g) *
+                             (std::fabs(st.v[i] - st.o) *
+                                  (1.0 + std::fabs(st.x[i]) + std::fabs(st.m)) +
+                              oerr);
+          if (dscore_err != nullptr) gsc_err[flat] = err;
+          if (dape_err != nullptr) dape_err[win[i].ape_index] += err + std::fabs(ds);
+          if (dape_abs != nullptr) dape_abs[win[i].ape_index] += std::fabs(ds);
+        }
+      }
+    }
+  }
+
+  for (int64_t i = 0; i < slots; ++i) {
+    if (count[i] > 1) return ORACLE_DOUBLE_WRITE;
+    dkv_bf16[i] = double_to_bf16_bits(gkv[i]);
+    dscore_bf16[i] = double_to_bf16_bits(gsc[i]);
+    if (dkv_f64 != nullptr) dkv_f64[i] = gkv[i];
+    if (dscore_f64 != nullptr) dscore_f64[i] = gsc[i];
+    if (owners != nullptr) owners[i] = count[i];
+    if (dscore_err != nullptr) dscore_err[i] = gsc_err[i];
+  }
+  if (dape_f32 != nullptr)
+    for (int64_t i = 0; i < static_cast<int64_t>(ratio) * C; ++i)
+      dape_f32[i] = static_cast<float>(dape_f64[i]);
+  return ORACLE_OK;
+}
+
+// Round doubles to bf16 bit patterns (exposed so the pins can test the rounding).
+void csa_oracle_round_bf16(const double* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = double_to_bf16_bits(x[i]);
+}
+
+}  // extern "C"
