@@ -1,0 +1,385 @@
+"""Benchmark: CSA/HCA compressor gated-softmax pooling, forward + backward, per THD pack.
+
+One step = csa_compressor_fwd + csa_compressor_bwd (the whole hot path) on one
+synthetic pack resident in HBM. Metric: fwd+bwd time and achieved HBM GB/s, where the
+bytes are the algorithmic ones (each consumed kv/score element read once, out/dout,
+the full dKV/dScore writes, ape and dAPE; workspace traffic is not counted).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run: each rank runs its own replica of the pack on
+its own GPU (the pooling has no cross-pack exchange), timing is the max over ranks, and
+the value is the bytes of all ranks over that time. Rank 0 prints one JSON line.
+--impl reference times the fp64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import thd_synth as ts  # noqa: E402
+
+METRIC = "fwd+bwd µs and achieved HBM GB/s (% of GB300 roofline) per THD pack"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------------
+# Algorithmic bytes
+# ----------------------------------------------------------------------------------
+
+def consumed_slots(pack) -> int:
+    lens = np.diff(pack.cu_seqlens.astype(np.int64))
+    n = lens // pack.ratio
+    if pack.coff == 2:
+        return int(np.sum(np.where(n >= 1, pack.d * pack.ratio * (2 * n - 1), 0)))
+    return int(np.sum(pack.d * pack.ratio * n))
+
+
+def algorithmic_bytes(pack):
+    ncons = consumed_slots(pack)
+    rc = pack.ratio * pack.C
+    reads = 2 * 2 * ncons + 4 * rc + 4 * (pack.S + 1)
+    fwd = reads + 2 * pack.total_comp * pack.d
+    bwd = reads + 2 * pack.total_comp * pack.d + 2 * 2 * pack.capacity * pack.C + 4 * rc
+    return fwd, bwd
+
+
+def workload_name(pack) -> str:
+    lens = np.diff(pack.cu_seqlens)
+    return (f"{pack.name}: THD pack S={pack.S} tokens={int(lens.sum())} capacity={pack.capacity} "
+            f"ratio={pack.ratio} coff={pack.coff} d={pack.d} total_comp={pack.total_comp}")
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------------
+# Clocks during the timed region
+# ----------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        mhz = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        maxm = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = sorted({n for r in rows for n, v in zip(self.NAMES, r[5:9])
+                          if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(maxm) if maxm else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import gated_pooling_gb300 as gp
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gp.load()
+    pack = ts.make_pack(args.config)
+    fwd_b, bwd_b = algorithmic_bytes(pack)
+    t = ts.to_torch(pack, dev)
+    S, r, coff, d, cap, TC, C = (pack.S, pack.ratio, pack.coff, pack.d, pack.capacity,
+                                 pack.total_comp, pack.C)
+    out = torch.empty((TC, d), dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty((cap, C), dtype=torch.bfloat16, device=dev)
+    dsc = torch.empty((cap, C), dtype=torch.bfloat16, device=dev)
+    dape = torch.empty((r, C), dtype=torch.float32, device=dev)
+    wsb = gp.csa_compressor_bwd_workspace_bytes(S, r, coff, d, cap, TC)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def fwd():
+        gp.csa_compressor_fwd(t["kv"], t["score"], t["ape"], t["cu_seqlens"], S, r, coff, d,
+                              cap, out, TC, err, stream=sp)
+
+    def bwd():
+        gp.csa_compressor_bwd(t["kv"], t["score"], t["ape"], t["cu_seqlens"], t["dout"], S, r,
+                              coff, d, cap, TC, dkv, dsc, dape, 0, ws, wsb, err, stream=sp)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid)
+                           if hasattr(torch.cuda.get_device_properties(dev), "uuid")
+                           else str(local_rank))
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()                   # L2 flush (256 MiB write), outside the events
+        ev[k][0].record(stream)
+        fwd()
+        ev[k][1].record(stream)
+        bwd()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
+    bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    tot = torch.tensor([sum(fwd_ms) + sum(bwd_ms), sum(fwd_ms), sum(bwd_ms)], dtype=torch.float64,
+                       device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
+    total_ms, fwd_total, bwd_total = (float(x) for x in tot.cpu())
+    ms_step = total_ms / args.steps
+    fwd_us = fwd_total / args.steps * 1e3
+    bwd_us = bwd_total / args.steps * 1e3
+    value = world * (fwd_b + bwd_b) / (ms_step * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers (copies inside the region)
+    e2e = run_e2e(args, pack, t, dev, fwd_b + bwd_b, wsb) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        return None
+
+    peak, peak_kind = measured_hbm_peak()
+    bwd_gbs = bwd_b / (bwd_us * 1e-6) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": workload_name(pack), "ratio": r, "coff": coff, "d": d, "S": S,
+                   "capacity": cap, "total_comp": TC,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "fwd_us": round(fwd_us, 2), "bwd_us": round(bwd_us, 2),
+        "fwd_bytes": fwd_b, "bwd_bytes": bwd_b,
+        "fwd_gbs": round(fwd_b / (fwd_us * 1e-6) / 1e9, 1), "bwd_gbs": round(bwd_gbs, 1),
+        "frac_of_measured_hbm": round(value / world / peak, 4),
+        "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "kernel": "csa_compressor_bwd (pooling backward + dAPE reduction)",
+                     "achieved": round(bwd_gbs, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(bwd_gbs / peak, 4), "traffic": None},
+        "e2e": e2e, "clocks": clocks, "gpu_launches": 3 * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(pack, budget_s=args.cpu_seconds)
+    return res
+
+
+def run_e2e(args, pack, t, dev, alg_bytes, wsb):
+    import torch
+    import gated_pooling_gb300 as gp
+
+    S, r, coff, d, cap, TC, C = (pack.S, pack.ratio, pack.coff, pack.d, pack.capacity,
+                                 pack.total_comp, pack.C)
+    host = {k: v.cpu().pin_memory() for k, v in t.items()}
+    dv = {k: torch.empty_like(v) for k, v in t.items()}
+    h_out = torch.empty((TC, d), dtype=torch.bfloat16).pin_memory()
+    h_dkv = torch.empty((cap, C), dtype=torch.bfloat16).pin_memory()
+    h_dsc = torch.empty((cap, C), dtype=torch.bfloat16).pin_memory()
+    h_dape = torch.empty((r, C), dtype=torch.float32).pin_memory()
+    out = torch.empty((TC, d), dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty((cap, C), dtype=torch.bfloat16, device=dev)
+    dsc = torch.empty((cap, C), dtype=torch.bfloat16, device=dev)
+    dape = torch.empty((r, C), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(x.numel() * x.element_size() for x in (h_out, h_dkv, h_dsc, h_dape))
+
+    def step():
+        for k in dv:
+            dv[k].copy_(host[k], non_blocking=True)
+        gp.csa_compressor_fwd(dv["kv"], dv["score"], dv["ape"], dv["cu_seqlens"], S, r, coff, d,
+                              cap, out, TC, None, stream=sp)
+        gp.csa_compressor_bwd(dv["kv"], dv["score"], dv["ape"], dv["cu_seqlens"], dv["dout"], S,
+                              r, coff, d, cap, TC, dkv, dsc, dape, 0, ws, wsb, None, stream=sp)
+        h_out.copy_(out, non_blocking=True)
+        h_dkv.copy_(dkv, non_blocking=True)
+        h_dsc.copy_(dsc, non_blocking=True)
+        h_dape.copy_(dape, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = args.e2e_steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    return {"value": round(alg_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ----------------------------------------------------------------------------------
+
+def sample_pack(pack, tokens: int):
+    """The first `tokens` tokens (a multiple of ratio) of the pack's first segment, as a
+    one-segment pack with the same ratio, coff, d and value streams."""
+    tokens = max(pack.ratio, min(tokens, int(pack.cu_seqlens[1]) - int(pack.cu_seqlens[0])))
+    tokens -= tokens % pack.ratio
+    c0 = int(pack.cu_seqlens[0])
+    n = tokens // pack.ratio
+    return ts.Pack(pack.name + f"[sample {tokens} tokens]", pack.ratio, pack.coff, pack.d, tokens,
+                   np.array([0, tokens], np.int32), pack.kv[c0:c0 + tokens],
+                   pack.score[c0:c0 + tokens], pack.ape, pack.dout[:n])
+
+
+def oracle_step_seconds(sp):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.fwd_pack(sp)
+    oracle.bwd_pack(sp)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(pack, budget_s=12.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of the pack."""
+    tokens = min(int(pack.cu_seqlens[1]) - int(pack.cu_seqlens[0]), 8192)
+    sp = sample_pack(pack, tokens)
+    fb, bb = algorithmic_bytes(sp)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while not times or (time.perf_counter() < t_end and len(times) < 20):
+        times.append(oracle_step_seconds(sp))
+    sec = statistics.median(times)
+    return {"value": round((fb + bb) / sec / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {sp.capacity} tokens of segment 0 ({sp.total_comp} output rows), "
+                      f"fwd+bwd x{len(times)}, median {sec:.3f} s per pass",
+            "sec_per_pass": round(sec, 4)}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    pack = ts.make_pack(args.config)
+    # size the per-step sample so the whole run stays within about two minutes
+    probe = sample_pack(pack, 64 * pack.ratio)
+    per_tok = oracle_step_seconds(probe) / probe.capacity
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    full = int(pack.cu_seqlens[1]) - int(pack.cu_seqlens[0])
+    tokens = int(max(pack.ratio, min(full, budget / max(per_tok, 1e-9))))
+    sp = sample_pack(pack, tokens)
+    fb, bb = algorithmic_bytes(sp)
+    for _ in range(args.warmup):
+        oracle_step_seconds(sp)
+    times = [oracle_step_seconds(sp) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = (fb + bb) / (ms * 1e-3) / 1e9
+    desc = (f"fp64 oracle, single thread, on the first {sp.capacity} tokens of segment 0 "
+            f"({sp.total_comp} output rows) per step")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(pack), "ratio": pack.ratio, "coff": pack.coff,
+                       "d": pack.d, "S": pack.S, "capacity": pack.capacity,
+                       "total_comp": pack.total_comp},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=ts.HEADLINE, choices=sorted(ts.SPECS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        res = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

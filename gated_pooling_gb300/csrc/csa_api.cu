@@ -1,0 +1,311 @@
+// csa_api.cu -- the C ABI of the GB300 CSA/HCA compressor pooling: argument checks,
+// launch planning, the index-map test hook and the fixed-order dAPE reduction.
+#include <climits>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "csa_compressor.h"
+#include "csa_internal.h"
+
+namespace csa {
+namespace {
+
+// Every launch runs on the current device. Multiprocessor counts and occupancies are
+// looked up once per (device, kernel, shared-memory size).
+struct OccEntry {
+  int dev;
+  const void* kernel;
+  size_t smem;
+  int blocks;
+};
+std::mutex g_mu;
+std::vector<OccEntry> g_occ;
+std::vector<int> g_sms;
+std::vector<std::pair<int, const void*>> g_attr_set;
+thread_local cudaError_t t_last_error = cudaSuccess;
+
+// Records a failing CUDA call for csa_last_error_string() and passes the code on.
+cudaError_t note(cudaError_t e) {
+  if (e != cudaSuccess) t_last_error = e;
+  return e;
+}
+
+cudaError_t device_sms(int dev, int* sms) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (dev < static_cast<int>(g_sms.size()) && g_sms[dev] > 0) {
+    *sms = g_sms[dev];
+    return cudaSuccess;
+  }
+  int n = 0;
+  cudaError_t e = note(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+  if (e != cudaSuccess) return e;
+  if (dev >= static_cast<int>(g_sms.size())) g_sms.resize(dev + 1, 0);
+  g_sms[dev] = n;
+  *sms = n;
+  return cudaSuccess;
+}
+
+// Blocks of `kernel` resident per SM with `smem` bytes of dynamic shared memory (0 if
+// it cannot run at all). Raises the kernel's dynamic shared-memory limit once.
+cudaError_t blocks_per_sm(int dev, const void* kernel, size_t smem, int* blocks) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const OccEntry& e : g_occ)
+    if (e.dev == dev && e.kernel == kernel && e.smem == smem) {
+      *blocks = e.blocks;
+      return cudaSuccess;
+    }
+  bool attr = false;
+  for (const auto& a : g_attr_set) attr = attr || (a.first == dev && a.second == kernel);
+  if (!attr) {
+    // The dynamic limit may reach the opt-in maximum less the kernel's static shared memory.
+    int optin = 0;
+    cudaError_t e = note(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = note(cudaFuncGetAttributes(&fa, kernel));
+    if (e != cudaSuccess) return e;
+    const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
+    e = note(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn));
+    if (e != cudaSuccess) return e;
+    g_attr_set.emplace_back(dev, kernel);
+  }
+  int n = 0;
+  cudaError_t e = note(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem));
+  if (e != cudaSuccess) return e;
+  g_occ.push_back({dev, kernel, smem, n});
+  *blocks = n;
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa_status_t check_sizes(int32_t S, int32_t ratio, int32_t coff, int32_t d, int64_t capacity,
+                         int64_t out_rows) {
+  if (S < 0 || ratio < 1 || d < 1 || capacity < 0 || out_rows < 0) return CSA_ERR_INVALID_VALUE;
+  if (coff != 1 && coff != 2) return CSA_ERR_UNSUPPORTED;
+  if (d % 8 != 0) return CSA_ERR_UNSUPPORTED;
+  if (S > CSA_MAX_SEGMENTS) return CSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(coff) * ratio > CSA_MAX_WINDOW) return CSA_ERR_UNSUPPORTED;
+  const int64_t C = static_cast<int64_t>(coff) * d;
+  if (C > INT_MAX / 8) return CSA_ERR_UNSUPPORTED;
+  if (capacity > 0 && capacity > INT_MAX / C) return CSA_ERR_UNSUPPORTED;
+  if (out_rows > 0 && out_rows > INT_MAX / d) return CSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(ratio) * C > INT_MAX) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+// Plan plus the device-dependent row-group count R.
+csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t d,
+                       int64_t out_rows, Plan* pl, PoolKernel* kernel) {
+  *pl = plan_shape(bwd, S, ratio, coff, d);
+  *kernel = bwd ? bwd_kernel_for(*pl) : fwd_kernel_for(*pl);
+  if (*kernel == nullptr) return CSA_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0, bps = 0;
+  if (note(cudaGetDevice(&dev)) != cudaSuccess) return CSA_ERR_CUDA;
+  if (device_sms(dev, &sms) != cudaSuccess) return CSA_ERR_CUDA;
+  if (blocks_per_sm(dev, reinterpret_cast<const void*>(*kernel), pl->smem, &bps) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  if (bps < 1) return CSA_ERR_UNSUPPORTED;  // shared memory of the plan does not fit
+  const int64_t want = (static_cast<int64_t>(sms) * bps + pl->K - 1) / pl->K;
+  const int64_t cap = out_rows > 0 ? out_rows : 1;
+  int64_t R = want < cap ? want : cap;
+  if (R < 1) R = 1;
+  if (R > 65535) R = 65535;
+  pl->R = static_cast<int>(R);
+  return CSA_OK;
+}
+
+PoolParams base_params(const Plan& pl, const void* kv, const void* score, const float* ape,
+                       const int32_t* cu, int32_t S, int32_t ratio, int32_t coff, int32_t d,
+                       int64_t capacity, int64_t out_rows, int32_t* dev_error) {
+  PoolParams p{};
+  p.kv = static_cast<const uint16_t*>(kv);
+  p.score = static_cast<const uint16_t*>(score);
+  p.ape = ape;
+  p.cu = cu;
+  p.dev_error = dev_error;
+  p.capacity = capacity;
+  p.out_rows = out_rows;
+  p.S = S;
+  p.r = ratio;
+  p.coff = coff;
+  p.d = d;
+  p.C = coff * d;
+  p.W = coff * ratio;
+  p.P = pl.P;
+  p.V = pl.V;
+  p.Vs = pl.Vs;
+  p.slots = pl.slots;
+  p.R = pl.R;
+  p.sB_words = pl.sB_words;
+  return p;
+}
+
+csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t stream) {
+  void* args[] = {&p};
+  cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
+                                        dim3(kThreads), args, pl.smem, stream));
+  return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+// dAPE = (accumulate ? dAPE : 0) + sum over row groups g = 0..R-1 of partial[g], the
+// sum taken in that order in fp64 and rounded to fp32 once.
+__global__ void dape_reduce_kernel(const float* __restrict__ partial, int R, int n,
+                                   float* __restrict__ dape, int accumulate) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  double s = 0.0;
+  for (int g = 0; g < R; ++g) s += static_cast<double>(partial[static_cast<int64_t>(g) * n + i]);
+  if (accumulate) s += static_cast<double>(dape[i]);
+  dape[i] = static_cast<float>(s);
+}
+
+__global__ void map_blocks_kernel(const int32_t* __restrict__ cu, int S, int ratio,
+                                  int64_t capacity, int64_t out_rows, int32_t* __restrict__ out,
+                                  int32_t* dev_error) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int warp_sums[32];
+  int* sB = reinterpret_cast<int*>(smem);
+  const int TC = build_block_prefix(cu, S, ratio, capacity, out_rows, dev_error, sB, warp_sums);
+  if (TC < 0) return;
+  for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < out_rows;
+       o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int32_t v0 = -1, v1 = -1, v2 = -1;
+    if (o < TC) {
+      const int s = find_segment(sB, S, static_cast<int>(o));
+      const int b = static_cast<int>(o) - sB[s];
+      v0 = s;
+      v1 = b;
+      v2 = __ldg(cu + s) + b * ratio;
+    }
+    out[3 * o + 0] = v0;
+    out[3 * o + 1] = v1;
+    out[3 * o + 2] = v2;
+  }
+}
+
+}  // namespace
+}  // namespace csa
+
+using namespace csa;
+
+extern "C" {
+
+const char* csa_status_string(int status) {
+  switch (status) {
+    case CSA_OK: return "CSA_OK";
+    case CSA_ERR_INVALID_VALUE: return "CSA_ERR_INVALID_VALUE: null, negative, misaligned or too small argument";
+    case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: coff not in {1,2}, d % 8 != 0, or a size limit exceeded";
+    case CSA_ERR_CUDA: return "CSA_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    default: return "unknown csa status";
+  }
+}
+
+const char* csa_last_error_string(void) {
+  return t_last_error == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(t_last_error);
+}
+
+int64_t csa_compressor_total_comp(const int32_t* cu, int32_t S, int32_t ratio) {
+  if (cu == nullptr || S < 0 || ratio < 1) return -1;
+  int64_t t = 0;
+  for (int32_t s = 0; s < S; ++s) {
+    if (cu[s + 1] < cu[s]) return -1;
+    t += (cu[s + 1] - cu[s]) / ratio;
+  }
+  return t;
+}
+
+csa_status_t csa_compressor_fwd(const void* kv, const void* score, const float* ape,
+                                const int32_t* cu_seqlens, int32_t S, int32_t ratio,
+                                int32_t coff, int32_t d, int64_t capacity, void* out,
+                                int64_t out_rows, int32_t* dev_error, csa_stream_t stream) {
+  csa_status_t st = check_sizes(S, ratio, coff, d, capacity, out_rows);
+  if (st != CSA_OK) return st;
+  if (cu_seqlens == nullptr || ape == nullptr) return CSA_ERR_INVALID_VALUE;
+  if (capacity > 0 && (kv == nullptr || score == nullptr)) return CSA_ERR_INVALID_VALUE;
+  if (out_rows > 0 && out == nullptr) return CSA_ERR_INVALID_VALUE;
+  if (!aligned16(kv) || !aligned16(score) || !aligned16(ape) || !aligned16(out))
+    return CSA_ERR_INVALID_VALUE;
+  Plan pl;
+  PoolKernel k;
+  st = make_plan(false, S, ratio, coff, d, out_rows, &pl, &k);
+  if (st != CSA_OK) return st;
+  PoolParams p = base_params(pl, kv, score, ape, cu_seqlens, S, ratio, coff, d, capacity,
+                             out_rows, dev_error);
+  p.out = static_cast<uint16_t*>(out);
+  return launch(k, pl, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t csa_compressor_bwd_workspace_bytes(int32_t S, int32_t ratio, int32_t coff, int32_t d,
+                                          int64_t capacity, int64_t out_rows) {
+  if (check_sizes(S, ratio, coff, d, capacity, out_rows) != CSA_OK) return 0;
+  Plan pl;
+  PoolKernel k;
+  if (make_plan(true, S, ratio, coff, d, out_rows, &pl, &k) != CSA_OK) return 0;
+  return static_cast<size_t>(pl.R) * ratio * coff * d * sizeof(float);
+}
+
+csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* ape,
+                                const int32_t* cu_seqlens, const void* dout, int32_t S,
+                                int32_t ratio, int32_t coff, int32_t d, int64_t capacity,
+                                int64_t out_rows, void* dkv, void* dscore, float* dape,
+                                int32_t accumulate_dape, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_error, csa_stream_t stream) {
+  csa_status_t st = check_sizes(S, ratio, coff, d, capacity, out_rows);
+  if (st != CSA_OK) return st;
+  if (cu_seqlens == nullptr || ape == nullptr || dape == nullptr) return CSA_ERR_INVALID_VALUE;
+  if (capacity > 0 && (kv == nullptr || score == nullptr || dkv == nullptr || dscore == nullptr))
+    return CSA_ERR_INVALID_VALUE;
+  if (out_rows > 0 && dout == nullptr) return CSA_ERR_INVALID_VALUE;
+  if (!aligned16(kv) || !aligned16(score) || !aligned16(ape) || !aligned16(dout) ||
+      !aligned16(dkv) || !aligned16(dscore) || !aligned16(dape) || !aligned16(workspace))
+    return CSA_ERR_INVALID_VALUE;
+  Plan pl;
+  PoolKernel k;
+  st = make_plan(true, S, ratio, coff, d, out_rows, &pl, &k);
+  if (st != CSA_OK) return st;
+  const size_t need = static_cast<size_t>(pl.R) * ratio * coff * d * sizeof(float);
+  if (workspace == nullptr || workspace_bytes < need) return CSA_ERR_INVALID_VALUE;
+  PoolParams p = base_params(pl, kv, score, ape, cu_seqlens, S, ratio, coff, d, capacity,
+                             out_rows, dev_error);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.dkv = static_cast<uint16_t*>(dkv);
+  p.dscore = static_cast<uint16_t*>(dscore);
+  p.partial = static_cast<float*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = launch(k, pl, p, s);
+  if (st != CSA_OK) return st;
+  const float* part = static_cast<const float*>(workspace);
+  int n = ratio * coff * d;
+  int R = pl.R;
+  int acc = accumulate_dape != 0;
+  void* rargs[] = {&part, &R, &n, &dape, &acc};
+  const cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(dape_reduce_kernel),
+                                              dim3((n + 255) / 256), dim3(256), rargs, 0, s));
+  return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+csa_status_t csa_compressor_map_blocks(const int32_t* cu_seqlens, int32_t S, int32_t ratio,
+                                       int64_t capacity, int64_t out_rows, int32_t* seg_blk_base,
+                                       int32_t* dev_error, csa_stream_t stream) {
+  if (cu_seqlens == nullptr || S < 0 || ratio < 1 || capacity < 0 || out_rows < 0)
+    return CSA_ERR_INVALID_VALUE;
+  if (out_rows > 0 && seg_blk_base == nullptr) return CSA_ERR_INVALID_VALUE;
+  if (S > CSA_MAX_SEGMENTS || out_rows > INT_MAX / 3) return CSA_ERR_UNSUPPORTED;
+  const int64_t blocks64 = (out_rows + kThreads - 1) / kThreads;
+  const int blocks = blocks64 < 1 ? 1 : (blocks64 > 1024 ? 1024 : static_cast<int>(blocks64));
+  const size_t smem = static_cast<size_t>((S + 1 + 3) & ~3) * sizeof(int);
+  int dev = 0, bps = 0;
+  if (note(cudaGetDevice(&dev)) != cudaSuccess) return CSA_ERR_CUDA;
+  if (blocks_per_sm(dev, reinterpret_cast<const void*>(map_blocks_kernel), smem, &bps) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  void* args[] = {const_cast<int32_t**>(&cu_seqlens), &S, &ratio, &capacity, &out_rows,
+                  &seg_blk_base, &dev_error};
+  const cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(map_blocks_kernel),
+                                              dim3(blocks), dim3(kThreads), args, smem,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+  return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+}  // extern "C"

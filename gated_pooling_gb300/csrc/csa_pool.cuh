@@ -1,0 +1,448 @@
+// csa_pool.cuh -- the pooling kernel of the GB300 CSA/HCA compressor, forward and
+// backward, and its launch planning.
+//
+// Operation ("Megatron-LM PR #5984", commit "CSA: add fused Compressor
+// forward+backward CuTe-DSL kernels"): per output row (one block of ratio tokens of
+// one THD segment) and column j < d, gather the window (coff=2: previous block at
+// column j, own block at column d+j; coff=1: own block at column j), add ape, take a
+// float32 softmax over the window positions, and sum kv with those weights; the
+// backward applies the softmax Jacobian, writes every dKV/dScore slot exactly once
+// (zeros where no window reads, commit "fold dKV/dScore zero-init into the backward
+// kernel") and sums dAPE without atomics.
+//
+// Work decomposition (one design for all window sizes):
+//   * A column "chunk" is VEC consecutive columns of one half (d/VEC chunks per half).
+//     A thread owns one chunk -- the same chunk in both halves at coff=2 -- and PP
+//     window positions (position group pg), for every row it visits. Window sizes
+//     W = coff*ratio > PP are split across P = ceil(W/PP) position groups whose
+//     per-column softmax partials (max, sum, weighted sum) are merged through shared
+//     memory in a fixed order.
+//   * A CTA is 256 threads = `slots` row slots x P groups x Vs chunks. gridDim.x = K
+//     column slices of Vs chunks, gridDim.y = R row groups; row group g owns output
+//     rows [g*TC/R, (g+1)*TC/R) (TC = total_comp, computed on the device), so every CTA
+//     gets the same number of rows to within one.
+//   * Every CTA rebuilds the segment -> block prefix from cu_seqlens into shared memory
+//     (the THD index map) and binary-searches it per row.
+//   * The ape values of the CTA's column slice are staged once in shared memory,
+//     pre-multiplied by log2(e): the softmax runs in base 2 (x' = score*log2e + ape').
+//   * Backward: per-thread dAPE sums stay in registers across rows; at the end the
+//     CTA adds its row slots in a fixed order and writes one partial per row group;
+//     a second kernel adds the R partials in a fixed order. No atomics anywhere.
+//   * Zero ownership (backward): the thread that processes a segment's last block
+//     zeroes that block's first-half columns (coff=2) and the segment's tail; segments
+//     with no block are zeroed by the row group whose row range holds their block
+//     offset; rows outside [cu[0], cu[S]) are split evenly across row groups.
+#pragma once
+
+#include <algorithm>
+
+#include "csa_device.cuh"
+
+namespace csa {
+
+constexpr int kThreads = 256;
+
+struct PoolParams {
+  const uint16_t* kv;     // bf16 [capacity, C]
+  const uint16_t* score;  // bf16 [capacity, C]
+  const float* ape;       // fp32 [r, C]
+  const int32_t* cu;      // int32 [S+1]
+  const uint16_t* dout;   // bf16 [out_rows, d]   (backward)
+  uint16_t* out;          // bf16 [out_rows, d]   (forward)
+  uint16_t* dkv;          // bf16 [capacity, C]   (backward)
+  uint16_t* dscore;       // bf16 [capacity, C]   (backward)
+  float* partial;         // fp32 [R, r, C]       (backward)
+  int32_t* dev_error;
+  int64_t capacity;
+  int64_t out_rows;
+  int S, r, coff, d, C, W;
+  int P;      // position groups
+  int V;      // chunks per half = d / VEC
+  int Vs;     // chunks per CTA column slice
+  int slots;  // row slots per CTA
+  int R;      // row groups = gridDim.y
+  int sB_words;  // ints reserved for the block prefix (>= S+1, multiple of 4)
+};
+
+// Zeroes rows [row0, row0+nrows) of dKV and dScore over this CTA's column slice (both
+// halves at coff=2). Cooperative over the whole CTA.
+template <int NW>
+__device__ __forceinline__ void zero_rows(const PoolParams& p, int64_t row0, int64_t nrows,
+                                          int slice_chunks) {
+  constexpr int VEC = 2 * NW;
+  const int per_row = slice_chunks * p.coff;
+  const int64_t items = nrows * per_row;
+  for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
+    const int64_t row = row0 + it / per_row;
+    const int rem = static_cast<int>(it % per_row);
+    const int half = rem / slice_chunks;
+    const int ch = blockIdx.x * p.Vs + rem % slice_chunks;
+    const int64_t off = row * p.C + half * p.d + ch * VEC;
+    store_zero<NW>(p.dkv + off);
+    store_zero<NW>(p.dscore + off);
+  }
+}
+
+// VEC: columns per chunk (8 forward, 4 backward). PP: window positions per thread.
+// SPLIT: windows span several position groups (P > 1).
+template <int VEC, int PP, bool BWD, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 2) pool_kernel(const PoolParams p) {
+  constexpr int NW = VEC / 2;  // 32-bit words per chunk
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int warp_sums[32];
+  int* sB = reinterpret_cast<int*>(smem);
+  float* sA = reinterpret_cast<float*>(sB + p.sB_words);   // [W][Vs*VEC], x log2(e)
+  float* sX = sA + p.W * p.Vs * VEC;                        // merge area / dAPE reduction
+
+  const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
+                                    warp_sums);
+  if (TC < 0) return;
+
+  const int tid = threadIdx.x;
+  const int r = p.r, d = p.d, C = p.C;
+  const bool two = p.coff == 2;
+  const int slice_w = p.Vs * VEC;  // columns per half in this slice (full slices)
+  const int slice_chunks = min(p.Vs, p.V - static_cast<int>(blockIdx.x) * p.Vs);
+
+  // Stage ape of this column slice, all window positions, scaled by log2(e).
+  for (int it = tid; it < p.W * p.Vs * (VEC / 4); it += blockDim.x) {
+    const int w = it / (p.Vs * (VEC / 4));
+    const int c4 = (it % (p.Vs * (VEC / 4))) * 4;     // column inside the slice
+    const int ch = blockIdx.x * p.Vs + c4 / VEC;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ch < p.V) {
+      const bool prev = two && w < r;
+      const int arow = (two && !prev) ? w - r : w;
+      const int col = ((two && !prev) ? d : 0) + blockIdx.x * slice_w + c4;
+      a = __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(arow) * C + col));
+    }
+    float* dst = sA + w * slice_w + c4;
+    dst[0] = a.x * kLog2e;
+    dst[1] = a.y * kLog2e;
+    dst[2] = a.z * kLog2e;
+    dst[3] = a.w * kLog2e;
+  }
+
+  const int tps = p.Vs * p.P;
+  const int slot = tid / tps;
+  const bool worker = slot < p.slots;
+  const int vl = tid % p.Vs;
+  const int pg = SPLIT ? (tid / p.Vs) % p.P : 0;
+  const int chunk = blockIdx.x * p.Vs + vl;
+  const bool col_ok = worker && chunk < p.V;
+  const int c0 = chunk * VEC;
+
+  const int g = blockIdx.y;
+  const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
+  const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
+
+  if constexpr (BWD) {
+    // Segments shorter than ratio: claimed by the row group whose range holds sB[s].
+    const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
+    const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
+    for (int s = s_lo; s < s_hi; ++s) {
+      const int a = __ldg(p.cu + s);
+      const int b = __ldg(p.cu + s + 1);
+      if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, slice_chunks);
+    }
+    // Rows outside [cu[0], cu[S]): an even share per row group.
+    const int64_t c_first = __ldg(p.cu);
+    const int64_t c_last = __ldg(p.cu + p.S);
+    const int64_t npad = c_first + (p.capacity - c_last);
+    const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
+    const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
+    const int64_t h0 = min(q1, c_first);                 // [q0, h0): rows before cu[0]
+    if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, slice_chunks);
+    const int64_t t0 = max(q0, c_first), t1 = q1;        // indices past cu[0] map to cu[S]+
+    if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, slice_chunks);
+  }
+  __syncthreads();  // sA ready
+
+  float acc[PP][VEC];  // backward: dAPE sums of this thread's positions and columns
+#pragma unroll
+  for (int i = 0; i < PP; ++i)
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) acc[i][c] = 0.f;
+
+  const int span = o1 - o0;
+  const int n_iter = (span + p.slots - 1) / p.slots;  // uniform over the CTA
+  for (int iter = 0; iter < n_iter; ++iter) {
+    const int o = o0 + iter * p.slots + slot;
+    const bool active = col_ok && o < o1;
+
+    int s = 0, b = 0, n = 1, cs = 0, ce = 0;
+    if (active) {
+      s = find_segment(sB, p.S, o);
+      b = o - sB[s];
+      n = sB[s + 1] - sB[s];
+      cs = __ldg(p.cu + s);
+      ce = __ldg(p.cu + s + 1);
+    }
+    const int base = cs + b * r;
+
+    // ---- gather the window slice of this thread --------------------------------
+    uint32_t kvw[PP][NW], scw[PP][NW];
+    int off[PP];
+    int aoff[PP];
+    bool valid[PP];
+#pragma unroll
+    for (int i = 0; i < PP; ++i) {
+      const int w = pg * PP + i;
+      const bool prev = two && w < r;
+      const int wo = (two && !prev) ? w - r : w;  // position inside the block read
+      bool v = active && w < p.W;
+      if (prev) v = v && b >= 1;
+      const int tok = prev ? base - r + w : base + wo;
+      const int col = ((two && !prev) ? d : 0) + c0;
+      valid[i] = v;
+      off[i] = tok * C + col;
+      aoff[i] = w * slice_w + vl * VEC;
+      if (v) {
+        load_stream<NW>(kvw[i], p.kv + off[i]);
+        load_stream<NW>(scw[i], p.score + off[i]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < NW; ++q) kvw[i][q] = scw[i][q] = 0u;
+      }
+    }
+    uint32_t gw[NW];
+    if constexpr (BWD) {
+      if (active) {
+        load_stream<NW>(gw, p.dout + static_cast<int64_t>(o) * d + c0);
+      } else {
+#pragma unroll
+        for (int q = 0; q < NW; ++q) gw[q] = 0u;
+      }
+    }
+
+    // ---- per-column softmax over this thread's positions (base 2) --------------
+    float m_loc[VEC], z_loc[VEC], a_loc[VEC];
+    float e[PP][VEC];
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      float x0[PP], x1[PP];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < PP; ++i) {
+        if (valid[i]) {
+          const float2 a = *reinterpret_cast<const float2*>(sA + aoff[i] + 2 * q);
+          x0[i] = fmaf(bf16_lo(scw[i][q]), kLog2e, a.x);
+          x1[i] = fmaf(bf16_hi(scw[i][q]), kLog2e, a.y);
+          mx0 = fmaxf(mx0, x0[i]);
+          mx1 = fmaxf(mx1, x1[i]);
+        } else {
+          x0[i] = x1[i] = -INFINITY;
+        }
+      }
+      float z0 = 0.f, z1 = 0.f, s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < PP; ++i) {
+        float e0 = 0.f, e1 = 0.f;
+        if (valid[i]) {
+          e0 = fast_exp2(x0[i] - mx0);
+          e1 = fast_exp2(x1[i] - mx1);
+        }
+        z0 += e0;
+        z1 += e1;
+        s0 = fmaf(e0, bf16_lo(kvw[i][q]), s0);
+        s1 = fmaf(e1, bf16_hi(kvw[i][q]), s1);
+        e[i][2 * q] = e0;
+        e[i][2 * q + 1] = e1;
+      }
+      m_loc[2 * q] = mx0;
+      m_loc[2 * q + 1] = mx1;
+      z_loc[2 * q] = z0;
+      z_loc[2 * q + 1] = z1;
+      a_loc[2 * q] = s0;
+      a_loc[2 * q + 1] = s1;
+    }
+
+    // ---- merge across position groups (fixed order) ----------------------------
+    float M[VEC], Z[VEC], A[VEC];
+    if constexpr (SPLIT) {
+      // partials: [3][blockDim][VEC]; finals: [3][slots*Vs][VEC]
+      float* pm = sX;
+      float* pz = pm + kThreads * VEC;
+      float* pa = pz + kThreads * VEC;
+      float* fm = pa + kThreads * VEC;
+      const int nfin = p.slots * p.Vs * VEC;
+      float* fz = fm + nfin;
+      float* fa = fz + nfin;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        pm[tid * VEC + c] = m_loc[c];
+        pz[tid * VEC + c] = z_loc[c];
+        pa[tid * VEC + c] = a_loc[c];
+      }
+      __syncthreads();
+      if (worker) {
+        for (int c = pg; c < VEC; c += p.P) {
+          float mm = -INFINITY, zz = 0.f, aa = 0.f;
+          for (int k = 0; k < p.P; ++k) {
+            const int src = (slot * p.P + k) * p.Vs + vl;
+            const float mk = pm[src * VEC + c];
+            if (mk == -INFINITY) continue;
+            const float mn = fmaxf(mm, mk);
+            const float so = fast_exp2(mm - mn);  // 0 while mm is -inf
+            const float sn = fast_exp2(mk - mn);
+            zz = __fadd_rn(__fmul_rn(zz, so), __fmul_rn(pz[src * VEC + c], sn));
+            aa = __fadd_rn(__fmul_rn(aa, so), __fmul_rn(pa[src * VEC + c], sn));
+            mm = mn;
+          }
+          const int dst = (slot * p.Vs + vl) * VEC + c;
+          fm[dst] = mm;
+          fz[dst] = zz;
+          fa[dst] = aa;
+        }
+      }
+      __syncthreads();
+      if (worker) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          const int src = (slot * p.Vs + vl) * VEC + c;
+          M[c] = fm[src];
+          Z[c] = fz[src];
+          A[c] = fa[src];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        M[c] = m_loc[c];
+        Z[c] = z_loc[c];
+        A[c] = a_loc[c];
+      }
+    }
+
+    if constexpr (!BWD) {
+      if (active && pg == 0) {
+        uint32_t ow[NW];
+#pragma unroll
+        for (int q = 0; q < NW; ++q) ow[q] = pack_bf16x2(A[2 * q] / Z[2 * q], A[2 * q + 1] / Z[2 * q + 1]);
+        store_stream<NW>(p.out + static_cast<int64_t>(o) * d + c0, ow);
+      }
+    } else {
+      // ---- softmax Jacobian: dKV = p*g, dScore = p*g*(kv - out) ------------------
+      float oc[VEC], qc[VEC], gc[VEC];
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        oc[c] = A[c] / Z[c];
+        const float scale = SPLIT ? fast_exp2(m_loc[c] - M[c]) : 1.f;
+        qc[c] = __fdiv_rn(scale, Z[c]);
+        gc[c] = (c & 1) ? bf16_hi(gw[c >> 1]) : bf16_lo(gw[c >> 1]);
+      }
+#pragma unroll
+      for (int i = 0; i < PP; ++i) {
+        if (!valid[i]) continue;
+        uint32_t dk[NW], ds[NW];
+#pragma unroll
+        for (int q = 0; q < NW; ++q) {
+          const float v0 = bf16_lo(kvw[i][q]), v1 = bf16_hi(kvw[i][q]);
+          const float k0 = (e[i][2 * q] * qc[2 * q]) * gc[2 * q];
+          const float k1 = (e[i][2 * q + 1] * qc[2 * q + 1]) * gc[2 * q + 1];
+          const float t0 = k0 * (v0 - oc[2 * q]);
+          const float t1 = k1 * (v1 - oc[2 * q + 1]);
+          acc[i][2 * q] += t0;
+          acc[i][2 * q + 1] += t1;
+          dk[q] = pack_bf16x2(k0, k1);
+          ds[q] = pack_bf16x2(t0, t1);
+        }
+        store_stream<NW>(p.dkv + off[i], dk);
+        store_stream<NW>(p.dscore + off[i], ds);
+      }
+      // ---- zeros owned by a segment's last block -----------------------------------
+      if (active && b == n - 1) {
+        if (two)  // first-half columns of the last block's own tokens
+          for (int k = pg; k < r; k += p.P) {
+            const int64_t offz = static_cast<int64_t>(base + k) * C + c0;
+            store_zero<NW>(p.dkv + offz);
+            store_zero<NW>(p.dscore + offz);
+          }
+        const int tail0 = cs + n * r;  // the segment's tail tokens, every half
+        for (int k = pg; k < ce - tail0; k += p.P) {
+          const int64_t offz = static_cast<int64_t>(tail0 + k) * C + c0;
+          store_zero<NW>(p.dkv + offz);
+          store_zero<NW>(p.dscore + offz);
+          if (two) {
+            store_zero<NW>(p.dkv + offz + d);
+            store_zero<NW>(p.dscore + offz + d);
+          }
+        }
+      }
+    }
+  }
+
+  if constexpr (BWD) {
+    // ---- dAPE: add the row slots in a fixed order, one partial per row group -------
+    float* red = sX;  // [PP*VEC][kThreads]
+    if (p.slots > 1) {
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < PP; ++i)
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) red[(i * VEC + c) * kThreads + tid] = acc[i][c];
+      __syncthreads();
+      if (slot == 0) {
+#pragma unroll
+        for (int i = 0; i < PP; ++i)
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) {
+            float sum = red[(i * VEC + c) * kThreads + tid];
+            for (int sl = 1; sl < p.slots; ++sl) sum += red[(i * VEC + c) * kThreads + sl * tps + tid];
+            acc[i][c] = sum;
+          }
+      }
+    }
+    if (slot == 0 && col_ok) {
+      float* dst = p.partial + static_cast<int64_t>(g) * r * C;
+#pragma unroll
+      for (int i = 0; i < PP; ++i) {
+        const int w = pg * PP + i;
+        if (w >= p.W) continue;
+        const bool prev = two && w < r;
+        const int arow = (two && !prev) ? w - r : w;
+        const int col = ((two && !prev) ? d : 0) + c0;
+        float* q = dst + static_cast<int64_t>(arow) * C + col;
+#pragma unroll
+        for (int c = 0; c < VEC; c += 4)
+          *reinterpret_cast<float4*>(q + c) = make_float4(acc[i][c], acc[i][c + 1], acc[i][c + 2], acc[i][c + 3]);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Launch planning (host)
+// ------------------------------------------------------------------------------------
+struct Plan {
+  int vec = 0, pp = 0, P = 0, V = 0, Vs = 0, slots = 0, K = 0, R = 0, sB_words = 0;
+  size_t smem = 0;
+  bool split = false;
+};
+
+inline int positions_per_thread(int W) { return W >= 5 ? 8 : (W >= 3 ? 4 : W); }
+
+// Geometry that does not depend on the device.
+inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
+  Plan pl;
+  pl.vec = bwd ? 4 : 8;
+  const int W = coff * r;
+  pl.pp = positions_per_thread(W);
+  pl.P = (W + pl.pp - 1) / pl.pp;
+  pl.split = pl.P > 1;
+  pl.V = d / pl.vec;
+  pl.Vs = std::min(pl.V, 32);
+  if (pl.split) pl.Vs = std::min(pl.Vs, std::max(1, kThreads / pl.P));
+  const int tps = pl.Vs * pl.P;
+  pl.slots = std::max(1, kThreads / tps);
+  pl.K = (pl.V + pl.Vs - 1) / pl.Vs;
+  pl.sB_words = ((S + 1) + 3) & ~3;
+  size_t x = 0;
+  if (pl.split)
+    x = std::max(x, (size_t)(3 * kThreads * pl.vec + 3 * pl.slots * pl.Vs * pl.vec) * sizeof(float));
+  if (bwd) x = std::max(x, (size_t)kThreads * pl.pp * pl.vec * sizeof(float));
+  pl.smem = (size_t)pl.sB_words * sizeof(int) + (size_t)W * pl.Vs * pl.vec * sizeof(float) + x;
+  return pl;
+}
+
+}  // namespace csa

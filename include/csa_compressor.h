@@ -1,0 +1,130 @@
+/*
+ * csa_compressor.h -- C ABI of the GB300 (sm_103a) CSA/HCA KV-compressor
+ * gated-softmax pooling over THD-packed ragged sequences.
+ *
+ * The operation (pages "Megatron-LM PR #5984", commit "CSA: add fused Compressor
+ * forward+backward CuTe-DSL kernels", and "cudnn-frontend PR #710"):
+ *
+ *   A pack holds S segments; segment s covers tokens [cu_seqlens[s], cu_seqlens[s+1]).
+ *   A segment of length L has floor(L / ratio) blocks of ratio consecutive tokens,
+ *   starting at the segment's first token; its last L mod ratio tokens belong to no
+ *   block. Output rows are the blocks of all segments in order (total_comp rows).
+ *   For block b of a segment and output column j < d, the window is:
+ *     coff=1: the block's own ratio tokens at column j;
+ *     coff=2: the previous block's ratio tokens at column j (absent for b = 0)
+ *             followed by the block's own ratio tokens at column d + j.
+ *   Each position adds ape[q, column read] to its score, q = the token's position in
+ *   its own block. A float32 softmax over the window positions weights kv, and the
+ *   weighted sum is rounded to bf16: out[row, j].
+ *   The backward gives dKV = p * dout and dScore = p * dout * (kv - out) at every slot
+ *   a window reads (out unrounded), +0 at every slot no window reads (the last
+ *   block's first-half columns at coff=2, tails, segments shorter than ratio, rows
+ *   outside [cu_seqlens[0], cu_seqlens[S])), and dAPE[q, col] = the sum of the
+ *   unrounded dScore terms that used ape[q, col].
+ *
+ * Conventions common to every entry point
+ *   - Every buffer belongs to the caller. The library allocates nothing, never
+ *     synchronises, and never reads device memory from the host.
+ *   - Work is enqueued on `stream` (NULL: the legacy default stream) of the current
+ *     device; calls return as soon as it is enqueued.
+ *   - bf16 tensors are row-major, contiguous, 16-byte aligned; ape is fp32, 16-byte
+ *     aligned. d must be a multiple of 8.
+ *   - Host-side argument checks return a status and enqueue nothing. Problems that
+ *     only the device can see (cu_seqlens decreasing, negative or past capacity;
+ *     more blocks than out_rows) make the kernels write a code to *dev_error (when
+ *     dev_error is not NULL), skip all output writes, and finish normally; outputs are
+ *     then unspecified. The library never clears *dev_error.
+ *   - Results are bitwise reproducible run to run (no atomics anywhere).
+ */
+#ifndef CSA_COMPRESSOR_H_
+#define CSA_COMPRESSOR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* csa_stream_t;
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_VALUE = 1, /* NULL pointer, negative size, misaligned pointer, small workspace */
+  CSA_ERR_UNSUPPORTED = 2,   /* coff not in {1,2}, d % 8 != 0, size limits below */
+  CSA_ERR_CUDA = 3           /* a CUDA runtime call or kernel launch failed */
+} csa_status_t;
+
+/* Codes the kernels write to *dev_error. */
+#define CSA_DEVERR_CU_SEQLENS 1 /* cu_seqlens[0] < 0, decreasing, or cu_seqlens[S] > capacity */
+#define CSA_DEVERR_OUT_ROWS 2   /* total_comp > out_rows */
+
+/* Limits checked on the host (CSA_ERR_UNSUPPORTED beyond them). */
+#define CSA_MAX_SEGMENTS 16384   /* S */
+#define CSA_MAX_WINDOW 2048      /* coff * ratio */
+#define CSA_MAX_ELEMS 2147483647 /* capacity*coff*d and out_rows*d must stay below 2^31 */
+
+/* Text for a status code (static storage). */
+const char* csa_status_string(int status);
+
+/* Text of the last CUDA runtime error a call of this library met on the calling host
+ * thread (why a call returned CSA_ERR_CUDA); static storage. */
+const char* csa_last_error_string(void);
+
+/* total_comp = sum over s of floor((cu[s+1] - cu[s]) / ratio), from a HOST copy of
+ * cu_seqlens [S+1]. Returns -1 when cu_seqlens is NULL, S < 0, ratio < 1 or the
+ * offsets decrease. Definition: "Megatron-LM PR #5984", commit "fold dKV/dScore
+ * zero-init into the backward kernel" (tails are seqlen mod ratio). */
+int64_t csa_compressor_total_comp(const int32_t* cu_seqlens_host, int32_t S, int32_t ratio);
+
+/* Forward pooling ("Megatron-LM PR #5984", commit "CSA: add fused Compressor
+ * forward+backward CuTe-DSL kernels"; coff=1 per commit "widen the validated
+ * envelope to coff in {1, 2}"; any ratio >= 1 per "cudnn-frontend PR #710").
+ *   kv, score   bf16 [capacity, coff*d] (device)
+ *   ape         fp32 [ratio, coff*d] (device)
+ *   cu_seqlens  int32 [S+1] (device), non-decreasing, cu_seqlens[S] <= capacity
+ *   out         bf16 [out_rows, d] (device); rows >= total_comp are not written
+ *   dev_error   int32 (device) or NULL
+ * S = 0 or out_rows = 0 with no block is a valid no-op. */
+csa_status_t csa_compressor_fwd(const void* kv, const void* score, const float* ape,
+                                const int32_t* cu_seqlens, int32_t S, int32_t ratio,
+                                int32_t coff, int32_t d, int64_t capacity, void* out,
+                                int64_t out_rows, int32_t* dev_error, csa_stream_t stream);
+
+/* Bytes of device workspace csa_compressor_bwd needs for these sizes on the current
+ * device (per-row-group dAPE partial sums; reduced in a fixed order). 0 on bad sizes. */
+size_t csa_compressor_bwd_workspace_bytes(int32_t S, int32_t ratio, int32_t coff, int32_t d,
+                                          int64_t capacity, int64_t out_rows);
+
+/* Backward pooling ("Megatron-LM PR #5984", commits "CSA: add fused Compressor
+ * forward+backward CuTe-DSL kernels" and "fold dKV/dScore zero-init into the
+ * backward kernel"). Inputs as for the forward, plus
+ *   dout        bf16 [out_rows, d] (device); rows >= total_comp are not read
+ *   dkv, dscore bf16 [capacity, coff*d] (device): EVERY element is written
+ *   dape        fp32 [ratio, coff*d] (device): accumulate_dape = 0 stores the sum,
+ *               1 adds it to the current contents
+ *   workspace   device scratch of at least csa_compressor_bwd_workspace_bytes(...)
+ *               bytes, 16-byte aligned; contents on entry do not matter
+ * Two kernels are enqueued: the pooling backward and a fixed-order dAPE reduction. */
+csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* ape,
+                                const int32_t* cu_seqlens, const void* dout, int32_t S,
+                                int32_t ratio, int32_t coff, int32_t d, int64_t capacity,
+                                int64_t out_rows, void* dkv, void* dscore, float* dape,
+                                int32_t accumulate_dape, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_error, csa_stream_t stream);
+
+/* Index map only (the THD segment/block mapping the pooling kernels use), for
+ * checking it bit for bit: for every output row o < out_rows writes
+ * seg_blk_base[3*o .. 3*o+2] = {segment, block inside the segment, first token of the
+ * block}, or {-1, -1, -1} when o >= total_comp. seg_blk_base: int32 [out_rows, 3],
+ * device. Reads cu_seqlens on the device like the pooling kernels. */
+csa_status_t csa_compressor_map_blocks(const int32_t* cu_seqlens, int32_t S, int32_t ratio,
+                                       int64_t capacity, int64_t out_rows, int32_t* seg_blk_base,
+                                       int32_t* dev_error, csa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_COMPRESSOR_H_ */

@@ -1,0 +1,123 @@
+"""The C-ABI library builds, loads and exports every entry point its header declares;
+host-side argument checks return the documented status codes. CPU only: no call
+here reaches the GPU (every call is rejected before any CUDA runtime call)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import gated_pooling_gb300 as gp
+import oracle
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "csa_compressor.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return gp.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\S[^\n(]*?\b(csa_\w+)\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(gp.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(4):
+        assert gp.csa_status_string(code).startswith("CSA_")
+
+
+def test_total_comp_host_helper(lib, oracle_lib):
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        S = int(rng.integers(0, 9))
+        cu = np.concatenate([[0], np.cumsum(rng.integers(0, 40, S))]).astype(np.int32)
+        r = int(rng.integers(1, 9))
+        assert gp.csa_compressor_total_comp(cu, S, r) == oracle.total_comp(cu, r)
+    assert gp.csa_compressor_total_comp(np.array([0, 5, 3], np.int32), 2, 2) == -1
+    assert gp.csa_compressor_total_comp(np.array([0], np.int32), 0, 0) == -1
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced (calls are rejected)
+
+
+def fwd_status(lib, **over):
+    a = dict(kv=FAKE, score=FAKE, ape=FAKE, cu=FAKE, S=1, ratio=4, coff=2, d=8, capacity=8,
+             out=FAKE, out_rows=2, err=None)
+    a.update(over)
+    return lib.csa_compressor_fwd(a["kv"], a["score"], a["ape"], a["cu"], a["S"], a["ratio"],
+                                  a["coff"], a["d"], a["capacity"], a["out"], a["out_rows"],
+                                  a["err"], None)
+
+
+def bwd_status(lib, **over):
+    a = dict(kv=FAKE, score=FAKE, ape=FAKE, cu=FAKE, dout=FAKE, S=1, ratio=4, coff=2, d=8,
+             capacity=8, out_rows=2, dkv=FAKE, dscore=FAKE, dape=FAKE, acc=0, ws=FAKE,
+             ws_bytes=1 << 20, err=None)
+    a.update(over)
+    return lib.csa_compressor_bwd(a["kv"], a["score"], a["ape"], a["cu"], a["dout"], a["S"],
+                                  a["ratio"], a["coff"], a["d"], a["capacity"], a["out_rows"],
+                                  a["dkv"], a["dscore"], a["dape"], a["acc"], a["ws"],
+                                  a["ws_bytes"], a["err"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(coff=0), gp.CSA_ERR_UNSUPPORTED),
+    (dict(coff=3), gp.CSA_ERR_UNSUPPORTED),
+    (dict(d=12), gp.CSA_ERR_UNSUPPORTED),
+    (dict(S=20000), gp.CSA_ERR_UNSUPPORTED),
+    (dict(ratio=2048), gp.CSA_ERR_UNSUPPORTED),          # window 4096 > 2048
+    (dict(capacity=1 << 28, d=64), gp.CSA_ERR_UNSUPPORTED),  # capacity*coff*d >= 2^31
+    (dict(out_rows=1 << 28, d=64), gp.CSA_ERR_UNSUPPORTED),
+    (dict(S=-1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(ratio=0), gp.CSA_ERR_INVALID_VALUE),
+    (dict(d=0), gp.CSA_ERR_INVALID_VALUE),
+    (dict(capacity=-1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(out_rows=-1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(cu=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(ape=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(kv=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(out=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(kv=FAKE + 8), gp.CSA_ERR_INVALID_VALUE),      # misaligned
+    (dict(out=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),
+])
+def test_fwd_rejects(lib, over, code):
+    assert fwd_status(lib, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(coff=3), gp.CSA_ERR_UNSUPPORTED),
+    (dict(d=4), gp.CSA_ERR_UNSUPPORTED),
+    (dict(dape=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(dkv=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(dscore=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(dout=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(dscore=FAKE + 4), gp.CSA_ERR_INVALID_VALUE),
+    (dict(ws=FAKE + 4), gp.CSA_ERR_INVALID_VALUE),
+    (dict(ratio=-2), gp.CSA_ERR_INVALID_VALUE),
+])
+def test_bwd_rejects(lib, over, code):
+    assert bwd_status(lib, **over) == code
+
+
+def test_workspace_query_rejects_bad_sizes(lib):
+    assert gp.csa_compressor_bwd_workspace_bytes(1, 4, 3, 8, 8, 2) == 0
+    assert gp.csa_compressor_bwd_workspace_bytes(1, 4, 2, 12, 8, 2) == 0
+
+
+def test_map_blocks_rejects(lib):
+    assert lib.csa_compressor_map_blocks(None, 1, 4, 8, 2, FAKE, None, None) == gp.CSA_ERR_INVALID_VALUE
+    assert lib.csa_compressor_map_blocks(FAKE, 1, 0, 8, 2, FAKE, None, None) == gp.CSA_ERR_INVALID_VALUE
+    assert lib.csa_compressor_map_blocks(FAKE, 1, 4, 8, 2, None, None, None) == gp.CSA_ERR_INVALID_VALUE

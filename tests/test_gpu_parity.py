@@ -1,0 +1,120 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Covers the five workload packs at full size (the launch configuration the bench
+times) and small packs that exercise every window shape the kernels specialise on:
+ragged packs, segments shorter than ratio, empty segments, tails, padding rows before
+cu_seqlens[0] and after cu_seqlens[S], coff 1 and 2, ratios 1..128, split windows,
+head dims whose chunk count does not fill a column slice, S = 0 and capacity 0.
+The tolerance is the one tests/parity.py derives; the count of elements that needed
+its cancellation clause is capped.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import thd_synth as ts
+from tests import gpu_harness as H
+from tests.parity import compare_bf16, compare_dape
+
+pytestmark = pytest.mark.gpu
+
+CLAUSE2_CAP = 2e-4  # fraction of elements allowed to need the cancellation clause
+
+
+def small_packs():
+    packs = {
+        "tiny": ts.make_pack("tiny"),
+        "r4c2_ragged_d16": ts.make_custom([1, 7, 0, 13, 4, 25], ratio=4, coff=2, d=16, pad_rows=5),
+        "r2c2_short_d64": ts.make_custom([1, 2, 3, 1, 9, 0, 5], ratio=2, coff=2, d=64, pad_rows=3),
+        "r3c2_d24": ts.make_custom([20, 5, 2], ratio=3, coff=2, d=24, pad_rows=2, seed=3),
+        "r1c1_d8": ts.make_custom([4, 0, 3], ratio=1, coff=1, d=8, pad_rows=1, seed=4),
+        "r1c2_d8": ts.make_custom([4, 1, 3], ratio=1, coff=2, d=8, pad_rows=2, seed=5),
+        "r4c1_d32": ts.make_custom([10, 3, 17], ratio=4, coff=1, d=32, pad_rows=4, seed=6),
+        "r8c1_d136": ts.make_custom([40, 17, 8], ratio=8, coff=1, d=136, pad_rows=3, seed=7),
+        "r4c2_d264": ts.make_custom([33, 9], ratio=4, coff=2, d=264, pad_rows=2, seed=8),
+        "r5c2_split_d16": ts.make_custom([31, 12, 4], ratio=5, coff=2, d=16, pad_rows=1, seed=9),
+        "r16c2_split_d32": ts.make_custom([70, 33, 15], ratio=16, coff=2, d=32, pad_rows=2, seed=10),
+        "r128c1_split_d64": ts.make_custom([300, 129, 50], ratio=128, coff=1, d=64, pad_rows=7,
+                                           seed=11, score_scale=4.0),
+        "r128c2_split_d32": ts.make_custom([400, 128, 127], ratio=128, coff=2, d=32, pad_rows=3,
+                                           seed=12),
+        "all_short": ts.make_custom([1, 2, 3], ratio=4, coff=2, d=8, pad_rows=2, seed=13),
+        "no_segments": ts.make_custom([], ratio=4, coff=2, d=8, pad_rows=5, seed=14),
+        "empty": ts.make_custom([], ratio=2, coff=1, d=8, pad_rows=0, seed=15),
+        "many_segments": ts.make_custom(list(np.random.default_rng(1).integers(0, 12, 700)),
+                                        ratio=4, coff=2, d=16, pad_rows=9, seed=16),
+    }
+    lead = ts.make_custom([6, 9, 14], ratio=4, coff=2, d=16, pad_rows=3, seed=17)
+    # same tensors with cu_seqlens starting at 6: rows 0..5 become padding, and the one
+    # block of the dropped first segment leaves dout
+    lead.cu_seqlens = np.ascontiguousarray(lead.cu_seqlens[1:])
+    lead.dout = np.ascontiguousarray(lead.dout[1:])
+    packs["lead_padding"] = lead
+    return packs
+
+
+SMALL = small_packs()
+FULL = ["tiny", "1x8192_d128", "3x8192_d512", "ragged_r2_d512", "long_r128_d512"]
+
+
+def check_fwd(gp, pack):
+    ref = oracle.fwd_pack(pack, want_f64=True, want_err=True)
+    got, err = H.run_fwd(gp, pack)
+    assert err == 0
+    rep = compare_bf16("out", got, ref["out"], ref["out_f64"], ref["out_err"])
+    print(pack.name, rep)
+    assert rep.fail == 0, str(rep)
+    assert rep.clause2 <= max(2, CLAUSE2_CAP * rep.n), str(rep)
+    return rep
+
+
+def check_bwd(gp, pack):
+    ref = oracle.bwd_pack(pack, want_f64=True, want_err=True, want_owners=True)
+    dkv, dsc, dape, err = H.run_bwd(gp, pack)
+    assert err == 0
+    r1 = compare_bf16("dkv", dkv, ref["dkv"], ref["dkv_f64"], np.abs(ref["dkv_f64"]))
+    r2 = compare_bf16("dscore", dsc, ref["dscore"], ref["dscore_f64"], ref["dscore_err"])
+    r3 = compare_dape(dape, ref["dape_f64"], ref["dape_err"])
+    print(pack.name, r1, r2, r3, sep="\n  ")
+    for rep in (r1, r2, r3):
+        assert rep.fail == 0, str(rep)
+    for rep in (r1, r2):
+        assert rep.clause2 <= max(2, CLAUSE2_CAP * rep.n), str(rep)
+    # never-consumed slots are exact +0
+    zero = ref["owners"] == 0
+    assert (dkv.reshape(ref["owners"].shape)[zero] == 0).all()
+    assert (dsc.reshape(ref["owners"].shape)[zero] == 0).all()
+    return r1, r2, r3
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_fwd_small(cuda_lib, name):
+    check_fwd(cuda_lib, SMALL[name])
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_bwd_small(cuda_lib, name):
+    check_bwd(cuda_lib, SMALL[name])
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_fwd_full(cuda_lib, name):
+    check_fwd(cuda_lib, ts.make_pack(name))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_bwd_full(cuda_lib, name):
+    check_bwd(cuda_lib, ts.make_pack(name))
+
+
+@pytest.mark.parametrize("name", ["tiny", "many_segments", "r4c2_ragged_d16", "no_segments"])
+def test_map_blocks_bit_exact(cuda_lib, name):
+    import torch
+    pack = SMALL[name]
+    rows = pack.total_comp + 3
+    out = torch.full((rows, 3), 7, dtype=torch.int32, device="cuda")
+    cu = torch.from_numpy(pack.cu_seqlens).cuda()
+    cuda_lib.csa_compressor_map_blocks(cu, pack.S, pack.ratio, pack.capacity, rows, out)
+    torch.cuda.synchronize()
+    want = oracle.map_blocks(pack.cu_seqlens, pack.ratio, rows)
+    assert (out.cpu().numpy() == want).all()

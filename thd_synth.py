@@ -193,3 +193,22 @@ def make_custom(lengths: List[int], ratio: int, coff: int, d: int, *, pad_rows: 
     spec = PackSpec("custom", list(lengths), ratio=ratio, coff=coff, d=d, pad_rows=pad_rows,
                     score_scale=score_scale, seed=seed)
     return make_pack(spec)
+
+
+def to_torch(pack: Pack, device="cuda") -> Dict[str, "object"]:
+    """Uploads a pack to torch tensors on ``device`` (bf16 tensors keep their bits)."""
+    import torch
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return {
+        "kv": bf(pack.kv).to(device),
+        "score": bf(pack.score).to(device),
+        "ape": torch.from_numpy(np.ascontiguousarray(pack.ape)).to(device),
+        "cu_seqlens": torch.from_numpy(np.ascontiguousarray(pack.cu_seqlens)).to(device),
+        "dout": bf(pack.dout).to(device),
+    }
+
+
+def bf16_tensor_bits(t) -> np.ndarray:
+    """uint16 bit patterns of a torch bf16 tensor (copied to the host)."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
