@@ -16,6 +16,7 @@ namespace {
 struct OccEntry {
   int dev;
   const void* kernel;
+  int threads;
   size_t smem;
   int blocks;
 };
@@ -48,10 +49,10 @@ cudaError_t device_sms(int dev, int* sms) {
 
 // Blocks of `kernel` resident per SM with `smem` bytes of dynamic shared memory (0 if
 // it cannot run at all). Raises the kernel's dynamic shared-memory limit once.
-cudaError_t blocks_per_sm(int dev, const void* kernel, size_t smem, int* blocks) {
+cudaError_t blocks_per_sm(int dev, const void* kernel, int threads, size_t smem, int* blocks) {
   std::lock_guard<std::mutex> lk(g_mu);
   for (const OccEntry& e : g_occ)
-    if (e.dev == dev && e.kernel == kernel && e.smem == smem) {
+    if (e.dev == dev && e.kernel == kernel && e.threads == threads && e.smem == smem) {
       *blocks = e.blocks;
       return cudaSuccess;
     }
@@ -71,9 +72,9 @@ cudaError_t blocks_per_sm(int dev, const void* kernel, size_t smem, int* blocks)
     g_attr_set.emplace_back(dev, kernel);
   }
   int n = 0;
-  cudaError_t e = note(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem));
+  cudaError_t e = note(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem));
   if (e != cudaSuccess) return e;
-  g_occ.push_back({dev, kernel, smem, n});
+  g_occ.push_back({dev, kernel, threads, smem, n});
   *blocks = n;
   return cudaSuccess;
 }
@@ -98,13 +99,19 @@ csa_status_t check_sizes(int32_t S, int32_t ratio, int32_t coff, int32_t d, int6
 // Plan plus the device-dependent row-group count R.
 csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t d,
                        int64_t out_rows, Plan* pl, PoolKernel* kernel) {
-  *pl = plan_shape(bwd, S, ratio, coff, d);
-  *kernel = bwd ? bwd_kernel_for(*pl) : fwd_kernel_for(*pl);
-  if (*kernel == nullptr) return CSA_ERR_UNSUPPORTED;
-  int dev = 0, sms = 0, bps = 0;
+  int dev = 0, sms = 0, bps = 0, optin = 0;
   if (note(cudaGetDevice(&dev)) != cudaSuccess) return CSA_ERR_CUDA;
   if (device_sms(dev, &sms) != cudaSuccess) return CSA_ERR_CUDA;
-  if (blocks_per_sm(dev, reinterpret_cast<const void*>(*kernel), pl->smem, &bps) != cudaSuccess)
+  if (note(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+      cudaSuccess)
+    return CSA_ERR_CUDA;
+  // Windows of <= 8 positions take the block-streaming kernel; longer ones the split kernel.
+  const size_t limit = static_cast<size_t>(optin) - 256;  // static shared memory headroom
+  if (!plan_stream(bwd, S, ratio, coff, d, limit, pl)) *pl = plan_shape(bwd, S, ratio, coff, d);
+  *kernel = bwd ? bwd_kernel_for(*pl) : fwd_kernel_for(*pl);
+  if (*kernel == nullptr) return CSA_ERR_UNSUPPORTED;
+  if (blocks_per_sm(dev, reinterpret_cast<const void*>(*kernel), pl->threads, pl->smem, &bps) !=
+      cudaSuccess)
     return CSA_ERR_CUDA;
   if (bps < 1) return CSA_ERR_UNSUPPORTED;  // shared memory of the plan does not fit
   const int64_t want = (static_cast<int64_t>(sms) * bps + pl->K - 1) / pl->K;
@@ -139,26 +146,62 @@ PoolParams base_params(const Plan& pl, const void* kv, const void* score, const 
   p.slots = pl.slots;
   p.R = pl.R;
   p.sB_words = pl.sB_words;
+  p.depth = pl.depth;
+  p.stage_bytes = pl.stage_bytes;
+  p.ape_off = pl.ape_off;
+  p.pre_off = pl.pre_off;
+  p.ring_off = pl.ring_off;
+  p.bar_off = pl.bar_off;
   return p;
 }
 
 csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t stream) {
   void* args[] = {&p};
   cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
-                                        dim3(kThreads), args, pl.smem, stream));
+                                        dim3(pl.threads), args, pl.smem, stream));
   return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
 
-// dAPE = (accumulate ? dAPE : 0) + sum over row groups g = 0..R-1 of partial[g], the
-// sum taken in that order in fp64 and rounded to fp32 once.
-__global__ void dape_reduce_kernel(const float* __restrict__ partial, int R, int n,
-                                   float* __restrict__ dape, int accumulate) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  double s = 0.0;
-  for (int g = 0; g < R; ++g) s += static_cast<double>(partial[static_cast<int64_t>(g) * n + i]);
-  if (accumulate) s += static_cast<double>(dape[i]);
-  dape[i] = static_cast<float>(s);
+// Neumaier's compensated summation step (Neumaier 1974): s + c carries the running sum
+// with the rounding error of every addition kept in c.
+__device__ __forceinline__ void neumaier_add(float& s, float& c, float x) {
+  const float t = s + x;
+  c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
+  s = t;
+}
+
+// dAPE = (accumulate ? dAPE : 0) + sum over row groups g = 0..R-1 of partial[g]. A block
+// covers 32 entries; its 8 warps each add a fixed contiguous range of row groups with
+// compensated fp32 sums, then warp 0 adds the 8 range sums in order. The result is the
+// same bits on every run.
+constexpr int kReduceCols = 32;
+constexpr int kReduceSplit = 8;
+__global__ void __launch_bounds__(kReduceCols * kReduceSplit)
+    dape_reduce_kernel(const float* __restrict__ partial, int R, int n, float* __restrict__ dape,
+                       int accumulate) {
+  __shared__ float s_sum[kReduceSplit][kReduceCols];
+  __shared__ float s_cmp[kReduceSplit][kReduceCols];
+  const int lane = threadIdx.x % kReduceCols;
+  const int k = threadIdx.x / kReduceCols;
+  const int e = blockIdx.x * kReduceCols + lane;
+  const int per = (R + kReduceSplit - 1) / kReduceSplit;
+  const int g0 = k * per;
+  const int g1 = min(R, g0 + per);
+  float s = 0.f, c = 0.f;
+  if (e < n)
+    for (int g = g0; g < g1; ++g) neumaier_add(s, c, partial[static_cast<int64_t>(g) * n + e]);
+  s_sum[k][lane] = s;
+  s_cmp[k][lane] = c;
+  __syncthreads();
+  if (k == 0 && e < n) {
+    float t = 0.f, tc = 0.f;
+    if (accumulate) neumaier_add(t, tc, dape[e]);
+    for (int kk = 0; kk < kReduceSplit; ++kk) {
+      neumaier_add(t, tc, s_sum[kk][lane]);
+      neumaier_add(t, tc, s_cmp[kk][lane]);
+    }
+    dape[e] = t + tc;
+  }
 }
 
 __global__ void map_blocks_kernel(const int32_t* __restrict__ cu, int S, int ratio,
@@ -282,7 +325,8 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
   int acc = accumulate_dape != 0;
   void* rargs[] = {&part, &R, &n, &dape, &acc};
   const cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(dape_reduce_kernel),
-                                              dim3((n + 255) / 256), dim3(256), rargs, 0, s));
+                                              dim3((n + kReduceCols - 1) / kReduceCols),
+                                              dim3(kReduceCols * kReduceSplit), rargs, 0, s));
   return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
 
@@ -298,7 +342,8 @@ csa_status_t csa_compressor_map_blocks(const int32_t* cu_seqlens, int32_t S, int
   const size_t smem = static_cast<size_t>((S + 1 + 3) & ~3) * sizeof(int);
   int dev = 0, bps = 0;
   if (note(cudaGetDevice(&dev)) != cudaSuccess) return CSA_ERR_CUDA;
-  if (blocks_per_sm(dev, reinterpret_cast<const void*>(map_blocks_kernel), smem, &bps) != cudaSuccess)
+  if (blocks_per_sm(dev, reinterpret_cast<const void*>(map_blocks_kernel), kThreads, smem, &bps) !=
+      cudaSuccess)
     return CSA_ERR_CUDA;
   void* args[] = {const_cast<int32_t**>(&cu_seqlens), &S, &ratio, &capacity, &out_rows,
                   &seg_blk_base, &dev_error};

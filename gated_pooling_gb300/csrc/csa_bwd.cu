@@ -1,10 +1,22 @@
 // csa_bwd.cu -- backward instantiations of the pooling kernel (4 columns per thread,
 // so that the per-thread dAPE sums fit in registers).
 #include "csa_internal.h"
+#include "csa_pool_stream.cuh"
 
 namespace csa {
 
 PoolKernel bwd_kernel_for(const Plan& pl) {
+  if (pl.tma) {
+    const int r = pl.pp / pl.coff, coff = pl.coff;
+    if (r == 1 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 1, 1, true>;
+    if (r == 2 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 2, 1, true>;
+    if (r == 4 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 4, 1, true>;
+    if (r == 8 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 8, 1, true>;
+    if (r == 1 && coff == 2) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 1, 2, true>;
+    if (r == 2 && coff == 2) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 2, 2, true>;
+    if (r == 4 && coff == 2) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 4, 2, true>;
+    return nullptr;
+  }
   if (pl.vec != 4) return nullptr;
   if (pl.split) return pl.pp == 8 ? pool_kernel<4, 8, true, true> : nullptr;
   switch (pl.pp) {

@@ -123,7 +123,8 @@ __device__ __forceinline__ int block_exclusive_scan(int val, int* warp_sums, int
 // *dev_error (if given) and every thread gets -1. Every thread of the block must call it.
 __device__ __forceinline__ int build_block_prefix(const int32_t* __restrict__ cu, int S,
                                                   int ratio, int64_t capacity, int64_t out_rows,
-                                                  int32_t* dev_error, int* sB, int* warp_sums) {
+                                                  int32_t* dev_error, int* sB, int* warp_sums,
+                                                  int* sCu = nullptr) {
   int carry = 0;
   int bad = 0;
   if (threadIdx.x == 0) {
@@ -137,6 +138,7 @@ __device__ __forceinline__ int build_block_prefix(const int32_t* __restrict__ cu
     if (s < S) {
       const int a = __ldg(cu + s);
       const int b = __ldg(cu + s + 1);
+      if (sCu != nullptr) sCu[s] = a;
       if (b < a) bad = 1;
       else n = (b - a) / ratio;
     }
@@ -145,7 +147,10 @@ __device__ __forceinline__ int build_block_prefix(const int32_t* __restrict__ cu
     if (s < S) sB[s] = carry + excl;
     carry += chunk_total;
   }
-  if (threadIdx.x == 0) sB[S] = carry;
+  if (threadIdx.x == 0) {
+    sB[S] = carry;
+    if (sCu != nullptr) sCu[S] = __ldg(cu + S);
+  }
   bad = __syncthreads_or(bad);
   int code = 0;
   if (bad) code = 1;                                       // CSA_DEVERR_CU_SEQLENS
@@ -169,6 +174,13 @@ __device__ __forceinline__ int find_segment(const int* sB, int S, int o) {
   return lo;
 }
 
+// Segment of row o given the segment `s` of an earlier row (rows visited in increasing
+// order): advances past segments that end at or before o.
+__device__ __forceinline__ int advance_segment(const int* sB, int s, int o) {
+  while (sB[s + 1] <= o) ++s;
+  return s;
+}
+
 // First s in [lo, hi) with sB[s] >= v (hi if none).
 __device__ __forceinline__ int lower_bound_prefix(const int* sB, int lo, int hi, int v) {
   while (lo < hi) {
@@ -177,6 +189,153 @@ __device__ __forceinline__ int lower_bound_prefix(const int* sB, int lo, int hi,
     else hi = mid;
   }
   return lo;
+}
+
+// ---------------------------------------------------------------------------------
+// Packed pairs of fp32 (two adjacent columns) for the sm_100-family f32x2 arithmetic:
+// every lane is an IEEE round-to-nearest fp32 operation, two per instruction.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) {
+  float lo;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(uint64_t v) {
+  float hi;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// A word of two bf16 (lower column in the low half) as an f32 pair (exact).
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// An f32 pair rounded to two bf16 (nearest even) in one word.
+__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) { return pack_bf16x2(f2_lo(v), f2_hi(v)); }
+// max of three fp32 (sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+}  // namespace csa
+
+namespace csa {
+
+// ---------------------------------------------------------------------------------
+// Bulk asynchronous copies (TMA, 1-D) completing on shared-memory mbarriers.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async proxy (the bulk-copy engine).
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned),
+// counted against `bar`'s transaction count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 16-byte shared-memory load that the compiler may not merge with an earlier load of the
+// same address (keeps re-reads from turning into long-lived registers).
+__device__ __forceinline__ uint4 lds128_fresh(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+// NW 32-bit words from shared memory (16 or 8 bytes, aligned). The _fresh form is never
+// merged with an earlier load of the same address.
+template <int NW>
+__device__ __forceinline__ void lds_words(uint32_t (&v)[NW], const void* p) {
+  if constexpr (NW == 4) {
+    const uint4 t = *reinterpret_cast<const uint4*>(p);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+    const uint2 t = *reinterpret_cast<const uint2*>(p);
+    v[0] = t.x; v[1] = t.y;
+  }
+}
+template <int NW>
+__device__ __forceinline__ void lds_words_fresh(uint32_t (&v)[NW], const void* p) {
+  if constexpr (NW == 4) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(smem_addr(p)));
+  } else {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(smem_addr(p)));
+  }
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the phase with `parity` of `bar` to complete, giving up after about
+// kWaitCycles SM clock cycles (returns false then). No wait in this library is unbounded.
+constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at GB300 clocks
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
 }
 
 }  // namespace csa

@@ -1,9 +1,21 @@
 // csa_fwd.cu -- forward instantiations of the pooling kernel (8 columns per thread).
 #include "csa_internal.h"
+#include "csa_pool_stream.cuh"
 
 namespace csa {
 
 PoolKernel fwd_kernel_for(const Plan& pl) {
+  if (pl.tma) {
+    const int r = pl.pp / pl.coff, coff = pl.coff;
+    if (r == 1 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 1, 1, false>;
+    if (r == 2 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 2, 1, false>;
+    if (r == 4 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 4, 1, false>;
+    if (r == 8 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 8, 1, false>;
+    if (r == 1 && coff == 2) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 1, 2, false>;
+    if (r == 2 && coff == 2) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 2, 2, false>;
+    if (r == 4 && coff == 2) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 4, 2, false>;
+    return nullptr;
+  }
   if (pl.vec != 8) return nullptr;
   if (pl.split) return pl.pp == 8 ? pool_kernel<8, 8, false, true> : nullptr;
   switch (pl.pp) {

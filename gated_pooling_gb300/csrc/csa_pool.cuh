@@ -62,17 +62,28 @@ struct PoolParams {
   int slots;  // row slots per CTA
   int R;      // row groups = gridDim.y
   int sB_words;  // ints reserved for the block prefix (>= S+1, multiple of 4)
+  // block-streaming kernel (csa_pool_stream.cuh) only
+  int depth;        // stages in the ring
+  int stage_bytes;  // bytes per stage
+  int ape_off;      // byte offsets in dynamic shared memory: staged ape,
+  int pre_off;      //   the block before the first row (left half),
+  int ring_off;     //   the ring of stages,
+  int bar_off;      //   the full/empty mbarriers
 };
 
 // Zeroes rows [row0, row0+nrows) of dKV and dScore over this CTA's column slice (both
 // halves at coff=2). Cooperative over the whole CTA.
 template <int NW>
 __device__ __forceinline__ void zero_rows(const PoolParams& p, int64_t row0, int64_t nrows,
-                                          int slice_chunks) {
+                                          int slice_chunks, int t0 = -1, int nt = 0) {
   constexpr int VEC = 2 * NW;
+  if (t0 < 0) {
+    t0 = threadIdx.x;
+    nt = blockDim.x;
+  }
   const int per_row = slice_chunks * p.coff;
   const int64_t items = nrows * per_row;
-  for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
+  for (int64_t it = t0; it < items; it += nt) {
     const int64_t row = row0 + it / per_row;
     const int rem = static_cast<int>(it % per_row);
     const int half = rem / slice_chunks;
@@ -418,6 +429,10 @@ struct Plan {
   int vec = 0, pp = 0, P = 0, V = 0, Vs = 0, slots = 0, K = 0, R = 0, sB_words = 0;
   size_t smem = 0;
   bool split = false;
+  bool tma = false;  // block-streaming kernel (bulk copies) for windows of <= 8 positions
+  int coff = 0;
+  int threads = kThreads;
+  int depth = 0, stage_bytes = 0, ape_off = 0, pre_off = 0, ring_off = 0, bar_off = 0;
 };
 
 inline int positions_per_thread(int W) { return W >= 5 ? 8 : (W >= 3 ? 4 : W); }
@@ -443,6 +458,73 @@ inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
   if (bwd) x = std::max(x, (size_t)kThreads * pl.pp * pl.vec * sizeof(float));
   pl.smem = (size_t)pl.sB_words * sizeof(int) + (size_t)W * pl.Vs * pl.vec * sizeof(float) + x;
   return pl;
+}
+
+// Block-streaming kernel shape: columns per thread and consumer threads, per direction.
+// The backward keeps 4 columns per thread so that its per-thread dAPE sums and softmax
+// weights stay in registers.
+#ifndef CSA_FWD_VEC
+#define CSA_FWD_VEC 8
+#endif
+#ifndef CSA_FWD_CONSUMERS
+#define CSA_FWD_CONSUMERS 256
+#endif
+#ifndef CSA_BWD_VEC
+#define CSA_BWD_VEC 4
+#endif
+#ifndef CSA_BWD_CONSUMERS
+#define CSA_BWD_CONSUMERS 256
+#endif
+
+// ratio/coff pairs the block-streaming kernel is instantiated for (window <= 8).
+inline bool stream_window_supported(int r, int coff) {
+  if (coff == 2) return r == 1 || r == 2 || r == 4;
+  return r == 1 || r == 2 || r == 4 || r == 8;
+}
+
+// Block-streaming kernel geometry: one CTA per SM, NC consumers + a producer warp, as many
+// stages as shared memory holds (<= 64), at least `slots + 2`. Returns false when the shape
+// does not fit it.
+inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
+  if (!stream_window_supported(r, coff)) return false;
+  const int W = coff * r;
+  const int vec = bwd ? CSA_BWD_VEC : CSA_FWD_VEC;
+  const int nc = bwd ? CSA_BWD_CONSUMERS : CSA_FWD_CONSUMERS;
+  if (d % vec != 0) return false;
+  Plan pl;
+  pl.tma = true;
+  pl.coff = coff;
+  pl.vec = vec;
+  pl.pp = W;
+  pl.P = 1;
+  pl.V = d / vec;
+  if (pl.V > nc) return false;
+  pl.Vs = pl.V;
+  pl.K = 1;
+  pl.slots = nc / pl.V;
+  pl.sB_words = ((S + 1) + 3) & ~3;
+  const size_t C = (size_t)coff * d;
+  pl.stage_bytes = (int)(2 * r * C * 2 + (bwd ? (size_t)d * 2 : 0));
+  const size_t ape_off = (size_t)pl.sB_words * 8;  // block prefix + cu_seqlens
+  const size_t pre_off = ape_off + (size_t)W * d * 4;
+  const size_t ring_off = (pre_off + (coff == 2 ? 2 * (size_t)r * d * 2 : 0) + 127) & ~(size_t)127;
+  const size_t red = bwd ? (size_t)W * vec * nc * 4 : 0;
+  if (smem_limit <= ring_off + 64) return false;
+  size_t depth = std::min<size_t>(64, (smem_limit - ring_off - 8) / (pl.stage_bytes + 16));
+  while (depth >= 3 && ring_off + std::max(depth * pl.stage_bytes, red) + (2 * depth + 1) * 8 >
+                           smem_limit)
+    --depth;
+  if (depth < 3) return false;
+  if ((size_t)pl.slots + 2 > depth) pl.slots = (int)depth - 2;  // keep the ring ahead of the consumers
+  pl.depth = (int)depth;
+  pl.threads = nc + 32;
+  pl.ape_off = (int)ape_off;
+  pl.pre_off = (int)pre_off;
+  pl.ring_off = (int)ring_off;
+  pl.bar_off = (int)(ring_off + std::max(depth * pl.stage_bytes, red));
+  pl.smem = (size_t)pl.bar_off + (2 * depth + 1) * 8;
+  *out = pl;
+  return true;
 }
 
 }  // namespace csa

@@ -1,0 +1,392 @@
+// csa_pool_stream.cuh -- block-streaming pooling kernel for windows of up to 8 positions
+// (the ratio=4 and ratio=2 coff=2 packs of the pages, and coff=1 up to ratio=8), forward
+// and backward.
+//
+// Same operation and zero ownership as pool_kernel (csa_pool.cuh). One CTA per SM owns a
+// contiguous range of output rows [o0, o1). Output row o is block b of segment s; its R
+// tokens are R consecutive rows of kv/score, so the block's full-width rows are ONE
+// contiguous range of R*C bf16 values. A producer warp streams, for each row of the
+// range in order, that block of kv and of score (and, backward, the dout row) into a
+// ring of shared-memory stages with 1-D bulk asynchronous copies (TMA), completing on
+// the stage's `full` mbarrier. The window of row o is the left half of stage o-1
+// (previous block, coff=2) and the right half of stage o (own block; the whole stage at
+// coff=1), so every consumed byte crosses HBM once. A stage is released (`empty`
+// mbarrier) once rows o and o+1 have read it. The block before o0 (read by row o0 when it
+// is not a segment's first block) is fetched once, left half only.
+//
+// Consumers (NC threads): a thread owns one chunk of VEC columns of a row, the same
+// chunk in both halves; NC/(d/VEC) rows are computed at once (row j -> row slot j mod
+// slots). Columns are processed in pairs with the f32x2 instructions. ratio and coff are
+// template parameters, so the window layout is static. No thread holds data in flight
+// in registers; every wait is bounded.
+#pragma once
+
+#include "csa_pool.cuh"
+
+namespace csa {
+
+// 1/z to within about one ulp: hardware approximation plus one Newton step.
+__device__ __forceinline__ float rcp_nr(float z) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(z));
+  const float e = fmaf(-z, r, 1.f);
+  return fmaf(r, e, r);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+template <int VEC, int NC, int R, int COFF, bool BWD>
+__global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParams p) {
+  constexpr int NW = VEC / 2;  // 32-bit words (= column pairs) per chunk
+  constexpr int NH = VEC / 4;  // float4 of ape per chunk
+  constexpr int W = R * COFF;
+  constexpr bool TWO = COFF == 2;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int warp_sums[32];
+  __shared__ int s_abort;
+  int* sB = reinterpret_cast<int*>(smem);                     // block prefix [S+1]
+  int* sCu = sB + p.sB_words;                                  // cu_seqlens [S+1]
+  const float4* sA = reinterpret_cast<const float4*>(smem + p.ape_off);  // [W][NH][V]
+  unsigned char* pre = smem + p.pre_off;                       // kv [R][d], score [R][d]
+  unsigned char* stages = smem + p.ring_off;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+  uint64_t* empty = full + p.depth;
+  uint64_t* pre_bar = empty + p.depth;
+
+  const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
+                                    warp_sums, sCu);
+  if (TC < 0) return;
+
+  const int tid = threadIdx.x;
+  const int d = p.d, C = p.C, V = p.V;
+  const int g = blockIdx.y;
+  const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
+  const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
+  const int nrows = o1 - o0;
+  const int kv_bytes = R * C * 2;  // one block of kv (or score), full width
+  const int stage_g = 2 * kv_bytes;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int i = 0; i < p.depth; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], COFF * V);
+    }
+    mbar_init(pre_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();  // barriers ready: the producer starts streaming right away
+
+  // does row o0 read a previous block (coff = 2 and not a segment's first block)?
+  bool need_pre = false;
+  if (TWO && nrows > 0) {
+    const int s = find_segment(sB, p.S, o0);
+    need_pre = o0 > sB[s];
+  }
+
+  uint64_t acc[W][NW];  // backward: dAPE sums, column pairs
+#pragma unroll
+  for (int i = 0; i < W; ++i)
+#pragma unroll
+    for (int q = 0; q < NW; ++q) acc[i][q] = 0ull;
+
+  if (tid >= NC) {
+    // ------------------------------ producer ------------------------------------------
+    if (tid == NC) {
+      int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
+      if (need_pre) {
+        const int base = sCu[s] + (o0 - sB[s] - 1) * R;
+        mbar_arrive_expect_tx(pre_bar, static_cast<uint32_t>(2 * R * d * 2));
+        for (int w = 0; w < R; ++w) {
+          const int64_t off = static_cast<int64_t>(base + w) * C;
+          bulk_load(pre + w * d * 2, p.kv + off, d * 2, pre_bar);
+          bulk_load(pre + (R + w) * d * 2, p.score + off, d * 2, pre_bar);
+        }
+      }
+      int j = 0;
+      for (; j < nrows; ++j) {
+        const int slot = j % p.depth;
+        if (j >= p.depth &&
+            !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>((j / p.depth - 1) & 1))) {
+          s_abort = 1;
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+        const int o = o0 + j;
+        s = advance_segment(sB, s, o);
+        const int base = sCu[s] + (o - sB[s]) * R;
+        unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_g + (BWD ? d * 2 : 0)));
+        const int64_t off = static_cast<int64_t>(base) * C;
+        bulk_load(st, p.kv + off, kv_bytes, &full[slot]);
+        bulk_load(st + kv_bytes, p.score + off, kv_bytes, &full[slot]);
+        if constexpr (BWD)
+          bulk_load(st + stage_g, p.dout + static_cast<int64_t>(o) * d, d * 2, &full[slot]);
+      }
+      if (j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) {
+        // stopping early: let every issued copy land before the CTA can exit
+        if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
+        for (int k = max(0, j - p.depth); k < j; ++k)
+          mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1));
+        if (need_pre) mbar_wait_bounded(pre_bar, 0);
+      }
+    }
+  } else {
+    // ------------------------------ consumers -----------------------------------------
+    // While the first stages are in flight: stage ape (scaled by log2 e) as
+    // [w][h][chunk] float4 (a chunk's float4s are V apart) and, backward, write the
+    // zeros of segments shorter than ratio and of the padding rows of this row group.
+    {
+      float4* dstA = reinterpret_cast<float4*>(smem + p.ape_off);
+      for (int it = tid; it < W * NH * V; it += NC) {
+        const int w = it / (NH * V);
+        const int h = (it / V) % NH;
+        const int ch = it % V;
+        const bool prev = TWO && w < R;
+        const int arow = (TWO && !prev) ? w - R : w;
+        const int col = ((TWO && !prev) ? d : 0) + ch * VEC + 4 * h;
+        float4 a =
+            __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(arow) * C + col));
+        a.x *= kLog2e;
+        a.y *= kLog2e;
+        a.z *= kLog2e;
+        a.w *= kLog2e;
+        dstA[it] = a;
+      }
+    }
+    if constexpr (BWD) {
+      const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
+      const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
+      for (int s = s_lo; s < s_hi; ++s) {
+        const int a = sCu[s];
+        const int b = sCu[s + 1];
+        if (b - a < R && b > a) zero_rows<NW>(p, a, b - a, V, tid, NC);
+      }
+      const int64_t c_first = sCu[0];
+      const int64_t c_last = sCu[p.S];
+      const int64_t npad = c_first + (p.capacity - c_last);
+      const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
+      const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
+      const int64_t h0 = min(q1, c_first);
+      if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, V, tid, NC);
+      const int64_t t0 = max(q0, c_first), t1 = q1;
+      if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, V, tid, NC);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");  // consumers only
+
+    const int rs = tid / V;  // row slot
+    const int vl = tid % V;  // chunk
+    const int c0 = vl * VEC;
+    const uint64_t kL2 = f2_pack(kLog2e, kLog2e);
+    if (rs < p.slots && rs < nrows) {
+      int s = find_segment(sB, p.S, o0 + rs);
+      for (int j = rs; j < nrows; j += p.slots) {
+        const int slot = j % p.depth;
+        const int o = o0 + j;
+        s = advance_segment(sB, s, o);
+        const int b = o - sB[s];
+        const int n = sB[s + 1] - sB[s];
+        const int cs = sCu[s];
+        const int base = cs + b * R;
+        const bool has_prev = TWO && b >= 1;
+        bool ok = mbar_wait_bounded(&full[slot], static_cast<uint32_t>((j / p.depth) & 1));
+        const unsigned char* own = stages + static_cast<size_t>(slot) * p.stage_bytes +
+                                   ((TWO ? d : 0) + c0) * 2;
+        const unsigned char* pkv = nullptr;  // previous block, left half, this chunk
+        int pstride = 0, psc = 0;            // its row stride and score offset (bytes)
+        if (has_prev) {
+          if (j == 0) {
+            ok = ok && mbar_wait_bounded(pre_bar, 0);
+            pkv = pre + c0 * 2;
+            pstride = d * 2;
+            psc = R * d * 2;
+          } else {
+            const int ps = (j - 1) % p.depth;
+            ok = ok && mbar_wait_bounded(&full[ps], static_cast<uint32_t>(((j - 1) / p.depth) & 1));
+            pkv = stages + static_cast<size_t>(ps) * p.stage_bytes + c0 * 2;
+            pstride = C * 2;
+            psc = kv_bytes;
+          }
+        }
+        if (!ok || *reinterpret_cast<volatile int*>(&s_abort)) {
+          s_abort = 1;
+          break;
+        }
+
+        // x' = score*log2e + ape*log2e, column pairs; masked positions are -inf
+        uint64_t x[W][NW];
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+          const bool prev = TWO && i < R;
+          if (prev && !has_prev) {
+#pragma unroll
+            for (int q = 0; q < NW; ++q) x[i][q] = f2_pack(-INFINITY, -INFINITY);
+            continue;
+          }
+          const unsigned char* sp =
+              prev ? pkv + psc + i * pstride : own + kv_bytes + (TWO ? i - R : i) * C * 2;
+          uint32_t sw[NW];
+          lds_words<NW>(sw, sp);
+          uint64_t a2[NW];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const float4 a = sA[(i * NH + h) * V + vl];
+            a2[2 * h] = f2_pack(a.x, a.y);
+            a2[2 * h + 1] = f2_pack(a.z, a.w);
+          }
+#pragma unroll
+          for (int q = 0; q < NW; ++q) x[i][q] = f2_fma(bf2_to_f2(sw[q]), kL2, a2[q]);
+        }
+        // negated column max, pairs
+        uint64_t nm[NW];
+#pragma unroll
+        for (int q = 0; q < NW; ++q) {
+          float mlo = f2_lo(x[0][q]), mhi = f2_hi(x[0][q]);
+#pragma unroll
+          for (int i = 1; i + 1 < W; i += 2) {
+            mlo = fmax3(mlo, f2_lo(x[i][q]), f2_lo(x[i + 1][q]));
+            mhi = fmax3(mhi, f2_hi(x[i][q]), f2_hi(x[i + 1][q]));
+          }
+          if constexpr (W % 2 == 0 && W > 1) {
+            mlo = fmaxf(mlo, f2_lo(x[W - 1][q]));
+            mhi = fmaxf(mhi, f2_hi(x[W - 1][q]));
+          }
+          nm[q] = f2_pack(-mlo, -mhi);
+        }
+        // e = 2^(x' - m), Z = sum e, A = sum e*kv
+        uint64_t z[NW], A[NW];
+#pragma unroll
+        for (int q = 0; q < NW; ++q) z[q] = A[q] = 0ull;
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+          const bool prev = TWO && i < R;
+          if (prev && !has_prev) {
+#pragma unroll
+            for (int q = 0; q < NW; ++q) x[i][q] = 0ull;
+            continue;
+          }
+          const unsigned char* kp = prev ? pkv + i * pstride : own + (TWO ? i - R : i) * C * 2;
+          uint32_t kw[NW];
+          lds_words<NW>(kw, kp);
+#pragma unroll
+          for (int q = 0; q < NW; ++q) {
+            const uint64_t dd = f2_add(x[i][q], nm[q]);
+            const uint64_t e2 = f2_pack(fast_exp2(f2_lo(dd)), fast_exp2(f2_hi(dd)));
+            z[q] = f2_add(z[q], e2);
+            A[q] = f2_fma(e2, bf2_to_f2(kw[q]), A[q]);
+            x[i][q] = e2;  // x now holds e
+          }
+        }
+        float rz[VEC];
+#pragma unroll
+        for (int q = 0; q < NW; ++q) {
+          rz[2 * q] = rcp_nr(f2_lo(z[q]));
+          rz[2 * q + 1] = rcp_nr(f2_hi(z[q]));
+        }
+
+        if constexpr (!BWD) {
+          uint32_t ow[NW];
+#pragma unroll
+          for (int q = 0; q < NW; ++q)
+            ow[q] = f2_to_bf2(f2_mul(A[q], f2_pack(rz[2 * q], rz[2 * q + 1])));
+          store_stream<NW>(p.out + static_cast<int64_t>(o) * d + c0, ow);
+        } else {
+          // p*g = e * (g / Z); dScore = p*g*(kv - out)
+          uint32_t gw[NW];
+          lds_words<NW>(gw, stages + static_cast<size_t>(slot) * p.stage_bytes + stage_g + c0 * 2);
+          uint64_t noc[NW], qg[NW];
+#pragma unroll
+          for (int q = 0; q < NW; ++q) {
+            noc[q] = f2_mul(A[q], f2_pack(-rz[2 * q], -rz[2 * q + 1]));
+            qg[q] = f2_mul(bf2_to_f2(gw[q]), f2_pack(rz[2 * q], rz[2 * q + 1]));
+          }
+#pragma unroll
+          for (int i = 0; i < W; ++i) {
+            const bool prev = TWO && i < R;
+            if (prev && !has_prev) continue;
+            const int tok = prev ? base - R + i : base + (TWO ? i - R : i);
+            const int64_t off = static_cast<int64_t>(tok) * C + ((TWO && !prev) ? d : 0) + c0;
+            const unsigned char* kp = prev ? pkv + i * pstride : own + (TWO ? i - R : i) * C * 2;
+            uint32_t kw[NW];
+            lds_words_fresh<NW>(kw, kp);
+            uint32_t dk[NW], ds[NW];
+#pragma unroll
+            for (int q = 0; q < NW; ++q) {
+              const uint64_t k2 = f2_mul(x[i][q], qg[q]);
+              const uint64_t t2 = f2_mul(k2, f2_add(bf2_to_f2(kw[q]), noc[q]));
+              acc[i][q] = f2_add(acc[i][q], t2);
+              dk[q] = f2_to_bf2(k2);
+              ds[q] = f2_to_bf2(t2);
+            }
+            store_stream<NW>(p.dkv + off, dk);
+            store_stream<NW>(p.dscore + off, ds);
+          }
+          if (b == n - 1) {  // zeros owned by a segment's last block
+            if (TWO) {
+#pragma unroll
+              for (int k = 0; k < R; ++k) {
+                const int64_t offz = static_cast<int64_t>(base + k) * C + c0;
+                store_zero<NW>(p.dkv + offz);
+                store_zero<NW>(p.dscore + offz);
+              }
+            }
+            const int ce = sCu[s + 1];
+            for (int t = cs + n * R; t < ce; ++t) {
+              const int64_t offz = static_cast<int64_t>(t) * C + c0;
+              store_zero<NW>(p.dkv + offz);
+              store_zero<NW>(p.dscore + offz);
+              if (TWO) {
+                store_zero<NW>(p.dkv + offz + d);
+                store_zero<NW>(p.dscore + offz + d);
+              }
+            }
+          }
+        }
+        // release the own stage and (coff=2) the previous one, which row o-1 also read
+        mbar_arrive(&empty[slot]);
+        if (TWO && j >= 1) mbar_arrive(&empty[(j - 1) % p.depth]);
+      }
+    }
+  }
+
+  if constexpr (BWD) {
+    // dAPE: add the row slots of each chunk in a fixed order, one partial per row group
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(stages);  // [W*VEC][NC]
+    if (tid < NC) {
+#pragma unroll
+      for (int i = 0; i < W; ++i)
+#pragma unroll
+        for (int q = 0; q < NW; ++q) {
+          red[(i * VEC + 2 * q) * NC + tid] = f2_lo(acc[i][q]);
+          red[(i * VEC + 2 * q + 1) * NC + tid] = f2_hi(acc[i][q]);
+        }
+    }
+    __syncthreads();
+    if (tid < V) {
+      const int c0 = tid * VEC;
+      float* dst = p.partial + static_cast<int64_t>(g) * R * C;
+#pragma unroll
+      for (int i = 0; i < W; ++i) {
+        float sum[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) sum[c] = 0.f;
+        for (int q = 0; q < p.slots; ++q)
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) sum[c] += red[(i * VEC + c) * NC + q * V + tid];
+        const bool prev = TWO && i < R;
+        const int arow = (TWO && !prev) ? i - R : i;
+        const int col = ((TWO && !prev) ? d : 0) + c0;
+        float* q = dst + static_cast<int64_t>(arow) * C + col;
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          *reinterpret_cast<float4*>(q + 4 * h) =
+              make_float4(sum[4 * h], sum[4 * h + 1], sum[4 * h + 2], sum[4 * h + 3]);
+      }
+    }
+  }
+}
+
+}  // namespace csa

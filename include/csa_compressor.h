@@ -59,6 +59,8 @@ typedef enum {
 /* Codes the kernels write to *dev_error. */
 #define CSA_DEVERR_CU_SEQLENS 1 /* cu_seqlens[0] < 0, decreasing, or cu_seqlens[S] > capacity */
 #define CSA_DEVERR_OUT_ROWS 2   /* total_comp > out_rows */
+#define CSA_DEVERR_TIMEOUT 3    /* a wait for an asynchronous copy gave up (about 2 s); the
+                                   kernel stopped early, outputs are incomplete */
 
 /* Limits checked on the host (CSA_ERR_UNSUPPORTED beyond them). */
 #define CSA_MAX_SEGMENTS 16384   /* S */
