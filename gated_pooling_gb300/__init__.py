@@ -24,7 +24,7 @@ CSA_OK, CSA_ERR_INVALID_VALUE, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA = 0, 1, 2, 3
 CSA_DEVERR_CU_SEQLENS, CSA_DEVERR_OUT_ROWS = 1, 2
 EXPORTED = ("csa_status_string", "csa_last_error_string", "csa_compressor_total_comp", "csa_compressor_fwd",
             "csa_compressor_bwd_workspace_bytes", "csa_compressor_bwd",
-            "csa_compressor_map_blocks")
+            "csa_compressor_bwd_noalloc", "csa_compressor_map_blocks")
 
 
 class CsaError(RuntimeError):
@@ -60,6 +60,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_compressor_bwd.restype = ctypes.c_int
     lib.csa_compressor_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i64, vp, vp,
                                        vp, i32, vp, sz, vp, vp]
+    lib.csa_compressor_bwd_noalloc.restype = ctypes.c_int
+    lib.csa_compressor_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i64,
+                                               vp, vp, vp, i32, vp, vp]
     lib.csa_compressor_map_blocks.restype = ctypes.c_int
     lib.csa_compressor_map_blocks.argtypes = [vp, i32, i32, i64, i64, vp, vp, vp]
     if path == LIB_PATH:
@@ -129,6 +132,18 @@ def csa_compressor_bwd(kv, score, ape, cu_seqlens, dout, S: int, ratio: int, cof
                                      _ptr(dscore), _ptr(dape), int(accumulate_dape),
                                      _ptr(workspace), workspace_bytes, _ptr(dev_error),
                                      _stream(stream)), "csa_compressor_bwd")
+
+
+def csa_compressor_bwd_noalloc(kv, score, ape, cu_seqlens, dout, S: int, ratio: int, coff: int,
+                               d: int, capacity: int, out_rows: int, dkv, dscore, dape,
+                               accumulate_dape: int, dev_error=None, stream=None) -> None:
+    """Backward without a caller workspace, for callers that cannot allocate device
+    memory; see include/csa_compressor.h for the shared scratch array's rules."""
+    _check(load().csa_compressor_bwd_noalloc(_ptr(kv), _ptr(score), _ptr(ape), _ptr(cu_seqlens),
+                                             _ptr(dout), S, ratio, coff, d, capacity, out_rows,
+                                             _ptr(dkv), _ptr(dscore), _ptr(dape),
+                                             int(accumulate_dape), _ptr(dev_error),
+                                             _stream(stream)), "csa_compressor_bwd_noalloc")
 
 
 def csa_compressor_map_blocks(cu_seqlens, S: int, ratio: int, capacity: int, out_rows: int,

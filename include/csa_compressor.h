@@ -116,6 +116,30 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
                                 int32_t accumulate_dape, void* workspace, size_t workspace_bytes,
                                 int32_t* dev_error, csa_stream_t stream);
 
+/* Size of the device scratch array csa_compressor_bwd_noalloc uses (4 MiB per GPU). */
+#define CSA_NOALLOC_SCRATCH_BYTES (4 << 20)
+
+/* Backward pooling for callers that cannot allocate device memory when they run it --
+ * for example code running inside an allocator or memory-pool callback (allocating there
+ * would re-enter the allocator), or a plugin in a host that reserves all device memory up
+ * front. The pages describe no such entry point; it is this library's addition. Same
+ * arguments and results as csa_compressor_bwd, without the workspace: the dAPE partial
+ * sums go to a file-scope device array of CSA_NOALLOC_SCRATCH_BYTES bytes that every GPU
+ * loading the library holds until the process unloads it. Nothing is allocated.
+ *   - Sizes whose workspace (csa_compressor_bwd_workspace_bytes) exceeds
+ *     CSA_NOALLOC_SCRATCH_BYTES are rejected with CSA_ERR_UNSUPPORTED, enqueueing nothing.
+ *   - The first call on a device (that device current) looks up the array's device
+ *     address once; make that first call before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero). Calls whose GPU work overlaps -- on
+ *     different streams or host threads of the same device -- race on it: order them. */
+csa_status_t csa_compressor_bwd_noalloc(const void* kv, const void* score, const float* ape,
+                                        const int32_t* cu_seqlens, const void* dout, int32_t S,
+                                        int32_t ratio, int32_t coff, int32_t d, int64_t capacity,
+                                        int64_t out_rows, void* dkv, void* dscore, float* dape,
+                                        int32_t accumulate_dape, int32_t* dev_error,
+                                        csa_stream_t stream);
+
 /* Index map only (the THD segment/block mapping the pooling kernels use), for
  * checking it bit for bit: for every output row o < out_rows writes
  * seg_blk_base[3*o .. 3*o+2] = {segment, block inside the segment, first token of the
