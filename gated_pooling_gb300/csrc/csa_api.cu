@@ -171,25 +171,27 @@ __device__ __forceinline__ void neumaier_add(float& s, float& c, float x) {
 }
 
 // dAPE = (accumulate ? dAPE : 0) + sum over row groups g = 0..R-1 of partial[g]. A block
-// covers 32 entries; its 8 warps each add a fixed contiguous range of row groups with
-// compensated fp32 sums, then warp 0 adds the 8 range sums in order. The result is the
-// same bits on every run.
+// covers 32 entries with 32 warps; warp k adds the contiguous row-group range
+// [k*R/32, (k+1)*R/32) (a few partials: their loads overlap) with compensated fp32 sums,
+// then warp 0 adds the 32 range sums in order. The result is the same bits on every
+// run. Launched as a programmatic dependent of the pooling kernel: it may start early
+// and waits for that grid's results.
 constexpr int kReduceCols = 32;
-constexpr int kReduceSplit = 8;
+constexpr int kReduceSplit = 32;
 __global__ void __launch_bounds__(kReduceCols * kReduceSplit)
     dape_reduce_kernel(const float* __restrict__ partial, int R, int n, float* __restrict__ dape,
                        int accumulate) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float s_sum[kReduceSplit][kReduceCols];
   __shared__ float s_cmp[kReduceSplit][kReduceCols];
   const int lane = threadIdx.x % kReduceCols;
   const int k = threadIdx.x / kReduceCols;
   const int e = blockIdx.x * kReduceCols + lane;
-  const int per = (R + kReduceSplit - 1) / kReduceSplit;
-  const int g0 = k * per;
-  const int g1 = min(R, g0 + per);
+  const int g_lo = static_cast<int>(static_cast<int64_t>(k) * R / kReduceSplit);
+  const int g_hi = static_cast<int>(static_cast<int64_t>(k + 1) * R / kReduceSplit);
   float s = 0.f, c = 0.f;
   if (e < n)
-    for (int g = g0; g < g1; ++g) neumaier_add(s, c, partial[static_cast<int64_t>(g) * n + e]);
+    for (int g = g_lo; g < g_hi; ++g) neumaier_add(s, c, __ldg(partial + static_cast<int64_t>(g) * n + e));
   s_sum[k][lane] = s;
   s_cmp[k][lane] = c;
   __syncthreads();
@@ -324,9 +326,18 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
   int R = pl.R;
   int acc = accumulate_dape != 0;
   void* rargs[] = {&part, &R, &n, &dape, &acc};
-  const cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(dape_reduce_kernel),
-                                              dim3((n + kReduceCols - 1) / kReduceCols),
-                                              dim3(kReduceCols * kReduceSplit), rargs, 0, s));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + kReduceCols - 1) / kReduceCols);
+  cfg.blockDim = dim3(kReduceCols * kReduceSplit);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      note(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(dape_reduce_kernel), rargs));
   return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
 

@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 2) pool_kernel(const PoolParams p) {
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums);
   if (TC < 0) return;
+  if constexpr (BWD) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tid = threadIdx.x;
   const int r = p.r, d = p.d, C = p.C;
@@ -463,17 +464,22 @@ inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
 // Block-streaming kernel shape: columns per thread and consumer threads, per direction.
 // The backward keeps 4 columns per thread so that its per-thread dAPE sums and softmax
 // weights stay in registers.
+#ifndef CSA_STREAM_CTAS
+#define CSA_STREAM_CTAS 1  // CTAs per SM
+#endif
+// Consumers plus one producer warp per CTA: 12 consumer warps + 1 producer keep at most
+// four warps per SM sub-partition (a 128-register budget per thread).
 #ifndef CSA_FWD_VEC
 #define CSA_FWD_VEC 8
 #endif
 #ifndef CSA_FWD_CONSUMERS
-#define CSA_FWD_CONSUMERS 256
+#define CSA_FWD_CONSUMERS 384
 #endif
 #ifndef CSA_BWD_VEC
 #define CSA_BWD_VEC 4
 #endif
 #ifndef CSA_BWD_CONSUMERS
-#define CSA_BWD_CONSUMERS 256
+#define CSA_BWD_CONSUMERS 384
 #endif
 
 // ratio/coff pairs the block-streaming kernel is instantiated for (window <= 8).
@@ -507,8 +513,10 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
   pl.stage_bytes = (int)(2 * r * C * 2 + (bwd ? (size_t)d * 2 : 0));
   const size_t ape_off = (size_t)pl.sB_words * 8;  // block prefix + cu_seqlens
   const size_t pre_off = ape_off + (size_t)W * d * 4;
-  const size_t ring_off = (pre_off + (coff == 2 ? 2 * (size_t)r * d * 2 : 0) + 127) & ~(size_t)127;
+  const size_t ring_off = (pre_off + (coff == 2 ? 2 * (size_t)r * C * 2 : 0) + 127) & ~(size_t)127;
   const size_t red = bwd ? (size_t)W * vec * nc * 4 : 0;
+  // CTAs per SM share the SM's 228 KiB (1 KiB reserved per CTA)
+  smem_limit = std::min<size_t>(smem_limit, (228 * 1024) / CSA_STREAM_CTAS - 1024 - 256);
   if (smem_limit <= ring_off + 64) return false;
   size_t depth = std::min<size_t>(64, (smem_limit - ring_off - 8) / (pl.stage_bytes + 16));
   while (depth >= 3 && ring_off + std::max(depth * pl.stage_bytes, red) + (2 * depth + 1) * 8 >

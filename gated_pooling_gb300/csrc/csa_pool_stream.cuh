@@ -12,7 +12,8 @@
 // (previous block, coff=2) and the right half of stage o (own block; the whole stage at
 // coff=1), so every consumed byte crosses HBM once. A stage is released (`empty`
 // mbarrier) once rows o and o+1 have read it. The block before o0 (read by row o0 when it
-// is not a segment's first block) is fetched once, left half only.
+// is not a segment's first block) is fetched once, left half only, into a buffer laid
+// out like a stage.
 //
 // Consumers (NC threads): a thread owns one chunk of VEC columns of a row, the same
 // chunk in both halves; NC/(d/VEC) rows are computed at once (row j -> row slot j mod
@@ -38,7 +39,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 template <int VEC, int NC, int R, int COFF, bool BWD>
-__global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParams p) {
+__global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(const PoolParams p) {
   constexpr int NW = VEC / 2;  // 32-bit words (= column pairs) per chunk
   constexpr int NH = VEC / 4;  // float4 of ape per chunk
   constexpr int W = R * COFF;
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
   int* sB = reinterpret_cast<int*>(smem);                     // block prefix [S+1]
   int* sCu = sB + p.sB_words;                                  // cu_seqlens [S+1]
   const float4* sA = reinterpret_cast<const float4*>(smem + p.ape_off);  // [W][NH][V]
-  unsigned char* pre = smem + p.pre_off;                       // kv [R][d], score [R][d]
+  unsigned char* pre = smem + p.pre_off;  // block before the first row: kv, score [R][C]
   unsigned char* stages = smem + p.ring_off;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.depth;
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
   const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
   if (TC < 0) return;
+  if constexpr (BWD) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tid = threadIdx.x;
   const int d = p.d, C = p.C, V = p.V;
@@ -95,14 +97,15 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
   if (tid >= NC) {
     // ------------------------------ producer ------------------------------------------
     if (tid == NC) {
+      const uint64_t pol = l2_evict_first_policy();
       int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
       if (need_pre) {
         const int base = sCu[s] + (o0 - sB[s] - 1) * R;
         mbar_arrive_expect_tx(pre_bar, static_cast<uint32_t>(2 * R * d * 2));
         for (int w = 0; w < R; ++w) {
           const int64_t off = static_cast<int64_t>(base + w) * C;
-          bulk_load(pre + w * d * 2, p.kv + off, d * 2, pre_bar);
-          bulk_load(pre + (R + w) * d * 2, p.score + off, d * 2, pre_bar);
+          bulk_load_hint(pre + w * C * 2, p.kv + off, d * 2, pre_bar, pol);
+          bulk_load_hint(pre + kv_bytes + w * C * 2, p.score + off, d * 2, pre_bar, pol);
         }
       }
       int j = 0;
@@ -120,10 +123,10 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
         unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
         mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_g + (BWD ? d * 2 : 0)));
         const int64_t off = static_cast<int64_t>(base) * C;
-        bulk_load(st, p.kv + off, kv_bytes, &full[slot]);
-        bulk_load(st + kv_bytes, p.score + off, kv_bytes, &full[slot]);
+        bulk_load_hint(st, p.kv + off, kv_bytes, &full[slot], pol);
+        bulk_load_hint(st + kv_bytes, p.score + off, kv_bytes, &full[slot], pol);
         if constexpr (BWD)
-          bulk_load(st + stage_g, p.dout + static_cast<int64_t>(o) * d, d * 2, &full[slot]);
+          bulk_load_hint(st + stage_g, p.dout + static_cast<int64_t>(o) * d, d * 2, &full[slot], pol);
       }
       if (j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) {
         // stopping early: let every issued copy land before the CTA can exit
@@ -192,22 +195,21 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
         const int base = cs + b * R;
         const bool has_prev = TWO && b >= 1;
         bool ok = mbar_wait_bounded(&full[slot], static_cast<uint32_t>((j / p.depth) & 1));
-        const unsigned char* own = stages + static_cast<size_t>(slot) * p.stage_bytes +
-                                   ((TWO ? d : 0) + c0) * 2;
-        const unsigned char* pkv = nullptr;  // previous block, left half, this chunk
-        int pstride = 0, psc = 0;            // its row stride and score offset (bytes)
+        // kv chunk of the own block's first token; score sits kv_bytes further, rows are C2
+        // bytes apart. The previous block (coff=2) uses the same layout (its own stage, or
+        // the block fetched before the first row).
+        const int C2 = C * 2;
+        const unsigned char* own_kv =
+            stages + static_cast<size_t>(slot) * p.stage_bytes + ((TWO ? d : 0) + c0) * 2;
+        const unsigned char* prev_kv = nullptr;
         if (has_prev) {
           if (j == 0) {
             ok = ok && mbar_wait_bounded(pre_bar, 0);
-            pkv = pre + c0 * 2;
-            pstride = d * 2;
-            psc = R * d * 2;
+            prev_kv = pre + c0 * 2;
           } else {
-            const int ps = (j - 1) % p.depth;
-            ok = ok && mbar_wait_bounded(&full[ps], static_cast<uint32_t>(((j - 1) / p.depth) & 1));
-            pkv = stages + static_cast<size_t>(ps) * p.stage_bytes + c0 * 2;
-            pstride = C * 2;
-            psc = kv_bytes;
+            const int pslot = (j - 1) % p.depth;
+            ok = ok && mbar_wait_bounded(&full[pslot], static_cast<uint32_t>(((j - 1) / p.depth) & 1));
+            prev_kv = stages + static_cast<size_t>(pslot) * p.stage_bytes + c0 * 2;
           }
         }
         if (!ok || *reinterpret_cast<volatile int*>(&s_abort)) {
@@ -215,20 +217,11 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
           break;
         }
 
-        // x' = score*log2e + ape*log2e, column pairs; masked positions are -inf
+        // x' = score*log2e + ape*log2e for window position i (column pairs)
         uint64_t x[W][NW];
-#pragma unroll
-        for (int i = 0; i < W; ++i) {
-          const bool prev = TWO && i < R;
-          if (prev && !has_prev) {
-#pragma unroll
-            for (int q = 0; q < NW; ++q) x[i][q] = f2_pack(-INFINITY, -INFINITY);
-            continue;
-          }
-          const unsigned char* sp =
-              prev ? pkv + psc + i * pstride : own + kv_bytes + (TWO ? i - R : i) * C * 2;
+        auto load_x = [&](const int i, const unsigned char* kvp) {
           uint32_t sw[NW];
-          lds_words<NW>(sw, sp);
+          lds_words<NW>(sw, kvp + kv_bytes);
           uint64_t a2[NW];
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
@@ -238,7 +231,21 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
           }
 #pragma unroll
           for (int q = 0; q < NW; ++q) x[i][q] = f2_fma(bf2_to_f2(sw[q]), kL2, a2[q]);
+        };
+        if constexpr (TWO) {
+          if (has_prev) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) load_x(i, prev_kv + i * C2);
+          } else {
+#pragma unroll
+            for (int i = 0; i < R; ++i)
+#pragma unroll
+              for (int q = 0; q < NW; ++q) x[i][q] = f2_pack(-INFINITY, -INFINITY);
+          }
         }
+#pragma unroll
+        for (int w = 0; w < R; ++w) load_x(W - R + w, own_kv + w * C2);
+
         // negated column max, pairs
         uint64_t nm[NW];
 #pragma unroll
@@ -255,35 +262,44 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
           }
           nm[q] = f2_pack(-mlo, -mhi);
         }
-        // e = 2^(x' - m), Z = sum e, A = sum e*kv
-        uint64_t z[NW], A[NW];
+
+        // e = 2^(x' - m); Z = sum e and A = sum e*kv, as two interleaved partial sums
+        uint64_t zz[2][NW], AA[2][NW];
 #pragma unroll
-        for (int q = 0; q < NW; ++q) z[q] = A[q] = 0ull;
-#pragma unroll
-        for (int i = 0; i < W; ++i) {
-          const bool prev = TWO && i < R;
-          if (prev && !has_prev) {
-#pragma unroll
-            for (int q = 0; q < NW; ++q) x[i][q] = 0ull;
-            continue;
-          }
-          const unsigned char* kp = prev ? pkv + i * pstride : own + (TWO ? i - R : i) * C * 2;
+        for (int q = 0; q < NW; ++q) zz[0][q] = zz[1][q] = AA[0][q] = AA[1][q] = 0ull;
+        auto acc_e = [&](const int i, const unsigned char* kvp) {
           uint32_t kw[NW];
-          lds_words<NW>(kw, kp);
+          lds_words<NW>(kw, kvp);
 #pragma unroll
           for (int q = 0; q < NW; ++q) {
             const uint64_t dd = f2_add(x[i][q], nm[q]);
             const uint64_t e2 = f2_pack(fast_exp2(f2_lo(dd)), fast_exp2(f2_hi(dd)));
-            z[q] = f2_add(z[q], e2);
-            A[q] = f2_fma(e2, bf2_to_f2(kw[q]), A[q]);
+            zz[i & 1][q] = f2_add(zz[i & 1][q], e2);
+            AA[i & 1][q] = f2_fma(e2, bf2_to_f2(kw[q]), AA[i & 1][q]);
             x[i][q] = e2;  // x now holds e
           }
+        };
+        if constexpr (TWO) {
+          if (has_prev) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) acc_e(i, prev_kv + i * C2);
+          } else {
+#pragma unroll
+            for (int i = 0; i < R; ++i)
+#pragma unroll
+              for (int q = 0; q < NW; ++q) x[i][q] = 0ull;
+          }
         }
+#pragma unroll
+        for (int w = 0; w < R; ++w) acc_e(W - R + w, own_kv + w * C2);
+        uint64_t A[NW];
         float rz[VEC];
 #pragma unroll
         for (int q = 0; q < NW; ++q) {
-          rz[2 * q] = rcp_nr(f2_lo(z[q]));
-          rz[2 * q + 1] = rcp_nr(f2_hi(z[q]));
+          const uint64_t z = f2_add(zz[0][q], zz[1][q]);
+          A[q] = f2_add(AA[0][q], AA[1][q]);
+          rz[2 * q] = rcp_nr(f2_lo(z));
+          rz[2 * q + 1] = rcp_nr(f2_hi(z));
         }
 
         if constexpr (!BWD) {
@@ -302,15 +318,10 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
             noc[q] = f2_mul(A[q], f2_pack(-rz[2 * q], -rz[2 * q + 1]));
             qg[q] = f2_mul(bf2_to_f2(gw[q]), f2_pack(rz[2 * q], rz[2 * q + 1]));
           }
-#pragma unroll
-          for (int i = 0; i < W; ++i) {
-            const bool prev = TWO && i < R;
-            if (prev && !has_prev) continue;
-            const int tok = prev ? base - R + i : base + (TWO ? i - R : i);
-            const int64_t off = static_cast<int64_t>(tok) * C + ((TWO && !prev) ? d : 0) + c0;
-            const unsigned char* kp = prev ? pkv + i * pstride : own + (TWO ? i - R : i) * C * 2;
+          const int64_t row_off = static_cast<int64_t>(base) * C + c0;  // own block, first half
+          auto grad = [&](const int i, const unsigned char* kvp, int64_t goff) {
             uint32_t kw[NW];
-            lds_words_fresh<NW>(kw, kp);
+            lds_words_fresh<NW>(kw, kvp);
             uint32_t dk[NW], ds[NW];
 #pragma unroll
             for (int q = 0; q < NW; ++q) {
@@ -320,16 +331,25 @@ __global__ void __launch_bounds__(NC + 32, 1) pool_stream_kernel(const PoolParam
               dk[q] = f2_to_bf2(k2);
               ds[q] = f2_to_bf2(t2);
             }
-            store_stream<NW>(p.dkv + off, dk);
-            store_stream<NW>(p.dscore + off, ds);
+            store_stream<NW>(p.dkv + goff, dk);
+            store_stream<NW>(p.dscore + goff, ds);
+          };
+          if constexpr (TWO) {
+            if (has_prev) {
+#pragma unroll
+              for (int i = 0; i < R; ++i)
+                grad(i, prev_kv + i * C2, row_off - static_cast<int64_t>(R - i) * C);
+            }
           }
+#pragma unroll
+          for (int w = 0; w < R; ++w)
+            grad(W - R + w, own_kv + w * C2, row_off + static_cast<int64_t>(w) * C + (TWO ? d : 0));
           if (b == n - 1) {  // zeros owned by a segment's last block
-            if (TWO) {
+            if constexpr (TWO) {
 #pragma unroll
               for (int k = 0; k < R; ++k) {
-                const int64_t offz = static_cast<int64_t>(base + k) * C + c0;
-                store_zero<NW>(p.dkv + offz);
-                store_zero<NW>(p.dscore + offz);
+                store_zero<NW>(p.dkv + row_off + static_cast<int64_t>(k) * C);
+                store_zero<NW>(p.dscore + row_off + static_cast<int64_t>(k) * C);
               }
             }
             const int ce = sCu[s + 1];
