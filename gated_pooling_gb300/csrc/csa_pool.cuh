@@ -467,19 +467,19 @@ inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
 #ifndef CSA_STREAM_CTAS
 #define CSA_STREAM_CTAS 1  // CTAs per SM
 #endif
-// Consumers plus one producer warp per CTA: 12 consumer warps + 1 producer keep at most
-// four warps per SM sub-partition (a 128-register budget per thread).
+// Consumers plus one producer warp per CTA: 8 consumer warps + 1 producer put at most
+// three warps on an SM sub-partition, a 168-register budget per thread (no spills).
 #ifndef CSA_FWD_VEC
 #define CSA_FWD_VEC 8
 #endif
 #ifndef CSA_FWD_CONSUMERS
-#define CSA_FWD_CONSUMERS 384
+#define CSA_FWD_CONSUMERS 256
 #endif
 #ifndef CSA_BWD_VEC
 #define CSA_BWD_VEC 4
 #endif
 #ifndef CSA_BWD_CONSUMERS
-#define CSA_BWD_CONSUMERS 384
+#define CSA_BWD_CONSUMERS 256
 #endif
 
 // ratio/coff pairs the block-streaming kernel is instantiated for (window <= 8).
