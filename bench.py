@@ -33,6 +33,11 @@ METRIC = "fwd+bwd µs and achieved HBM GB/s (% of GB300 roofline) per THD pack"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+# DRAM bytes (read + write) per backward call on the headline pack, from one ncu capture
+# of this build: pool kernel 108.28 MB read + 47.77 MB write (the rest of its writes are
+# still dirty in L2 when it ends), reduction 2.50 MB read. Summarised in
+# profiles/pool_stream_kernel_3x8192_d512.md; it must be re-measured when a kernel changes.
+ROOFLINE_TRAFFIC = {"3x8192_d512": 108.281088e6 + 47.766016e6 + 2.49856e6}
 
 
 # ----------------------------------------------------------------------------------
@@ -250,7 +255,8 @@ def run_ours(args, rank, world, local_rank):
         "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "kernel": "csa_compressor_bwd (pooling backward + dAPE reduction)",
                      "achieved": round(bwd_gbs, 1), "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": round(bwd_gbs / peak, 4), "traffic": None},
+                     "unit": "GB/s", "frac": round(bwd_gbs / peak, 4),
+                     "traffic": ROOFLINE_TRAFFIC.get(args.config)},
         "e2e": e2e, "clocks": clocks, "gpu_launches": 3 * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline:
