@@ -35,8 +35,8 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) per backward call on the headline pack, from one ncu capture
 # of this build: pool kernel 108.28 MB read + 47.77 MB write (the rest of its writes are
-# still dirty in L2 when it ends), reduction 2.50 MB read. Summarised in
-# profiles/pool_stream_kernel_3x8192_d512.md; it must be re-measured when a kernel changes.
+# still dirty in L2 when it ends), reduction 2.50 MB read (the capture's summary is kept
+# with the profiles). It must be re-measured whenever a kernel changes.
 ROOFLINE_TRAFFIC = {"3x8192_d512": 108.281088e6 + 47.766016e6 + 2.49856e6}
 
 
@@ -74,6 +74,24 @@ def measured_hbm_peak():
             return float(json.load(fh)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------------
+# Multi-rank aggregation (replicas: one pack per GPU, no data-path collective)
+# ----------------------------------------------------------------------------------
+
+def max_over_ranks(values, device="cpu"):
+    """Element-wise max of `values` over all ranks (identity without a process group)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_gbs(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Bytes all ranks moved per step over the slowest rank's step time, in GB/s."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------------------------------
@@ -196,15 +214,12 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop() if rank == 0 else None
     fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
-    tot = torch.tensor([sum(fwd_ms) + sum(bwd_ms), sum(fwd_ms), sum(bwd_ms)], dtype=torch.float64,
-                       device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
-    total_ms, fwd_total, bwd_total = (float(x) for x in tot.cpu())
+    total_ms, fwd_total, bwd_total = max_over_ranks(
+        [sum(fwd_ms) + sum(bwd_ms), sum(fwd_ms), sum(bwd_ms)], device=dev)
     ms_step = total_ms / args.steps
     fwd_us = fwd_total / args.steps * 1e3
     bwd_us = bwd_total / args.steps * 1e3
-    value = world * (fwd_b + bwd_b) / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, fwd_b + bwd_b, ms_step)
 
     # context: the same two calls captured once in a CUDA graph and replayed
     graph_us = None
