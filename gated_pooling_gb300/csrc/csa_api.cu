@@ -107,7 +107,9 @@ csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t
     return CSA_ERR_CUDA;
   // Windows of <= 8 positions take the block-streaming kernel; longer ones the split kernel.
   const size_t limit = static_cast<size_t>(optin) - 256;  // static shared memory headroom
-  if (!plan_stream(bwd, S, ratio, coff, d, limit, pl)) *pl = plan_shape(bwd, S, ratio, coff, d);
+  if (!(!bwd && plan_fwd_ldg(S, ratio, coff, d, limit, pl)) &&
+      !plan_stream(bwd, S, ratio, coff, d, limit, pl))
+    *pl = plan_shape(bwd, S, ratio, coff, d);
   *kernel = bwd ? bwd_kernel_for(*pl) : fwd_kernel_for(*pl);
   if (*kernel == nullptr) return CSA_ERR_UNSUPPORTED;
   if (blocks_per_sm(dev, reinterpret_cast<const void*>(*kernel), pl->threads, pl->smem, &bps) !=

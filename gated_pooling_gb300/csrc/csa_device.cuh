@@ -23,6 +23,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 1/z to within about one ulp: hardware approximation plus one Newton step.
+__device__ __forceinline__ float rcp_nr(float z) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(z));
+  const float e = fmaf(-z, r, 1.f);
+  return fmaf(r, e, r);
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22; x = -inf gives 0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -1,10 +1,22 @@
 // csa_fwd.cu -- forward instantiations of the pooling kernel (8 columns per thread).
 #include "csa_internal.h"
+#include "csa_fwd_ldg.cuh"
 #include "csa_pool_stream.cuh"
 
 namespace csa {
 
 PoolKernel fwd_kernel_for(const Plan& pl) {
+  if (pl.ldg) {
+    const int r = pl.pp / pl.coff, coff = pl.coff;
+    if (r == 1 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 1, 1>;
+    if (r == 2 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 2, 1>;
+    if (r == 4 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 4, 1>;
+    if (r == 8 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 8, 1>;
+    if (r == 1 && coff == 2) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 1, 2>;
+    if (r == 2 && coff == 2) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 2, 2>;
+    if (r == 4 && coff == 2) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 4, 2>;
+    return nullptr;
+  }
   if (pl.tma) {
     const int r = pl.pp / pl.coff, coff = pl.coff;
     if (r == 1 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 1, 1, false>;

@@ -1,0 +1,163 @@
+// csa_fwd_ldg.cuh -- forward pooling through register loads, for windows of up to 8
+// positions (same operation as csa_pool_stream.cuh; "Megatron-LM PR #5984", commit "CSA:
+// add fused Compressor forward+backward CuTe-DSL kernels").
+//
+// The forward reads ~95% of its bytes. Streaming reads through bulk copies into shared
+// memory top out lower on GB300 than plain evict-first vector loads into registers with
+// enough of them in flight, so this variant keeps everything in registers: each thread
+// owns one chunk of 4 columns of a row (both halves at coff=2) and loads, per row, the
+// 2*W 8-byte pieces of its window (kv and score) itself. The loads of the thread's next
+// row are issued before the current row is computed (a register double buffer), so every
+// thread always has a row in flight. CTAs are persistent (one per SM, or two) and own a
+// contiguous range of rows, split over their row slots.
+#pragma once
+
+#include "csa_pool.cuh"
+
+namespace csa {
+
+template <int NT, int R, int COFF>
+__global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const PoolParams p) {
+  constexpr int VEC = 4, NW = 2, NH = 1;
+  constexpr int W = R * COFF;
+  constexpr bool TWO = COFF == 2;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int warp_sums[32];
+  int* sB = reinterpret_cast<int*>(smem);
+  int* sCu = sB + p.sB_words;
+  float4* sA = reinterpret_cast<float4*>(smem + p.ape_off);  // [W][V] float4, x log2(e)
+
+  const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
+                                    warp_sums, sCu);
+  if (TC < 0) return;
+
+  const int tid = threadIdx.x;
+  const int d = p.d, C = p.C, V = p.V;
+  const int g = blockIdx.y;
+  const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
+  const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
+  const int nrows = o1 - o0;
+
+  for (int it = tid; it < W * V; it += NT) {
+    const int w = it / V;
+    const int ch = it % V;
+    const bool prev = TWO && w < R;
+    const int arow = (TWO && !prev) ? w - R : w;
+    const int col = ((TWO && !prev) ? d : 0) + ch * VEC;
+    float4 a = __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(arow) * C + col));
+    a.x *= kLog2e;
+    a.y *= kLog2e;
+    a.z *= kLog2e;
+    a.w *= kLog2e;
+    sA[it] = a;
+  }
+  __syncthreads();
+
+  const int rs = tid / V;
+  const int vl = tid % V;
+  const int c0 = vl * VEC;
+  if (rs >= p.slots || rs >= nrows) return;
+  const uint64_t kL2 = f2_pack(kLog2e, kLog2e);
+
+  // window of row o for this chunk: kv and score words of the W positions (masked
+  // positions of a segment's first block stay zero and are flagged by has_prev = false)
+  int seg = find_segment(sB, p.S, o0 + rs);
+  auto fetch = [&](const int j, uint32_t (&kv)[W][NW], uint32_t (&sc)[W][NW], bool& has_prev) {
+    const int o = o0 + j;
+    seg = advance_segment(sB, seg, o);
+    const int b = o - sB[seg];
+    has_prev = TWO && b >= 1;
+    const int64_t own = (static_cast<int64_t>(sCu[seg]) + static_cast<int64_t>(b) * R) * C +
+                        (TWO ? d : 0) + c0;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const bool prev = TWO && i < R;
+      if (prev && !has_prev) {
+#pragma unroll
+        for (int q = 0; q < NW; ++q) kv[i][q] = sc[i][q] = 0u;
+        continue;
+      }
+      const int64_t off = prev ? own - d - static_cast<int64_t>(R - i) * C
+                               : own + static_cast<int64_t>(TWO ? i - R : i) * C;
+      load_stream<NW>(kv[i], p.kv + off);
+      load_stream<NW>(sc[i], p.score + off);
+    }
+  };
+
+  uint32_t kv[W][NW], sc[W][NW];
+  bool hp = false;
+  fetch(rs, kv, sc, hp);
+  for (int j = rs; j < nrows; j += p.slots) {
+    uint32_t kvn[W][NW], scn[W][NW];
+    bool hpn = false;
+    const bool more = j + p.slots < nrows;
+    if (more) fetch(j + p.slots, kvn, scn, hpn);
+
+    uint64_t x[W][NW];
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const bool prev = TWO && i < R;
+      if (prev && !hp) {
+#pragma unroll
+        for (int q = 0; q < NW; ++q) x[i][q] = f2_pack(-INFINITY, -INFINITY);
+        continue;
+      }
+      const float4 a = sA[i * V + vl];
+      const uint64_t a2[2] = {f2_pack(a.x, a.y), f2_pack(a.z, a.w)};
+#pragma unroll
+      for (int q = 0; q < NW; ++q) x[i][q] = f2_fma(bf2_to_f2(sc[i][q]), kL2, a2[q]);
+    }
+    uint64_t nm[NW];
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      float mlo = f2_lo(x[0][q]), mhi = f2_hi(x[0][q]);
+#pragma unroll
+      for (int i = 1; i + 1 < W; i += 2) {
+        mlo = fmax3(mlo, f2_lo(x[i][q]), f2_lo(x[i + 1][q]));
+        mhi = fmax3(mhi, f2_hi(x[i][q]), f2_hi(x[i + 1][q]));
+      }
+      if constexpr (W % 2 == 0 && W > 1) {
+        mlo = fmaxf(mlo, f2_lo(x[W - 1][q]));
+        mhi = fmaxf(mhi, f2_hi(x[W - 1][q]));
+      }
+      nm[q] = f2_pack(-mlo, -mhi);
+    }
+    uint64_t zz[2][NW], AA[2][NW];
+#pragma unroll
+    for (int q = 0; q < NW; ++q) zz[0][q] = zz[1][q] = AA[0][q] = AA[1][q] = 0ull;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const bool prev = TWO && i < R;
+      if (prev && !hp) continue;
+#pragma unroll
+      for (int q = 0; q < NW; ++q) {
+        const uint64_t dd = f2_add(x[i][q], nm[q]);
+        const uint64_t e2 = f2_pack(fast_exp2(f2_lo(dd)), fast_exp2(f2_hi(dd)));
+        zz[i & 1][q] = f2_add(zz[i & 1][q], e2);
+        AA[i & 1][q] = f2_fma(e2, bf2_to_f2(kv[i][q]), AA[i & 1][q]);
+      }
+    }
+    uint32_t ow[NW];
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      const uint64_t z = f2_add(zz[0][q], zz[1][q]);
+      const uint64_t A = f2_add(AA[0][q], AA[1][q]);
+      ow[q] = f2_to_bf2(f2_mul(A, f2_pack(rcp_nr(f2_lo(z)), rcp_nr(f2_hi(z)))));
+    }
+    store_stream<NW>(p.out + static_cast<int64_t>(o0 + j) * d + c0, ow);
+
+    if (more) {
+#pragma unroll
+      for (int i = 0; i < W; ++i)
+#pragma unroll
+        for (int q = 0; q < NW; ++q) {
+          kv[i][q] = kvn[i][q];
+          sc[i][q] = scn[i][q];
+        }
+      hp = hpn;
+    }
+  }
+  (void)NH;
+}
+
+}  // namespace csa

@@ -431,6 +431,7 @@ struct Plan {
   size_t smem = 0;
   bool split = false;
   bool tma = false;  // block-streaming kernel (bulk copies) for windows of <= 8 positions
+  bool ldg = false;  // forward through register loads (csa_fwd_ldg.cuh)
   int coff = 0;
   int threads = kThreads;
   int depth = 0, stage_bytes = 0, ape_off = 0, pre_off = 0, ring_off = 0, bar_off = 0;
@@ -482,6 +483,16 @@ inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
 #define CSA_BWD_CONSUMERS 256
 #endif
 
+#ifndef CSA_FWD_LDG
+#define CSA_FWD_LDG 1      // forward windows <= 8 through register loads
+#endif
+#ifndef CSA_LDG_THREADS
+#define CSA_LDG_THREADS 512
+#endif
+#ifndef CSA_LDG_CTAS
+#define CSA_LDG_CTAS 1
+#endif
+
 // ratio/coff pairs the block-streaming kernel is instantiated for (window <= 8).
 inline bool stream_window_supported(int r, int coff) {
   if (coff == 2) return r == 1 || r == 2 || r == 4;
@@ -531,6 +542,36 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
   pl.ring_off = (int)ring_off;
   pl.bar_off = (int)(ring_off + std::max(depth * pl.stage_bytes, red));
   pl.smem = (size_t)pl.bar_off + (2 * depth + 1) * 8;
+  *out = pl;
+  return true;
+}
+
+// Register-load forward geometry: 4 columns per thread, CSA_LDG_THREADS threads per CTA,
+// rows split over NT/(d/4) row slots. Returns false when the shape does not fit it.
+// Measured on GB300: register loads win for windows of <= 4 positions and for narrow rows
+// (d < 512), where the bulk-copy pipeline's start-up dominates; the block-streaming kernel
+// wins for 8-position windows of wide rows (the headline ratio=4 coff=2 d=512 pack).
+inline bool fwd_prefers_ldg(int r, int coff, int d) { return coff * r <= 4 || d < 512; }
+
+inline bool plan_fwd_ldg(int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
+  if (!CSA_FWD_LDG || !stream_window_supported(r, coff) || d % 4 != 0) return false;
+  if (!fwd_prefers_ldg(r, coff, d)) return false;
+  Plan pl;
+  pl.ldg = true;
+  pl.coff = coff;
+  pl.vec = 4;
+  pl.pp = coff * r;
+  pl.P = 1;
+  pl.V = d / 4;
+  if (pl.V > CSA_LDG_THREADS) return false;
+  pl.Vs = pl.V;
+  pl.K = 1;
+  pl.slots = CSA_LDG_THREADS / pl.V;
+  pl.sB_words = ((S + 1) + 3) & ~3;
+  pl.ape_off = pl.sB_words * 8;
+  pl.smem = (size_t)pl.ape_off + (size_t)coff * r * d * 4;
+  if (pl.smem > smem_limit) return false;
+  pl.threads = CSA_LDG_THREADS;
   *out = pl;
   return true;
 }

@@ -26,14 +26,6 @@
 
 namespace csa {
 
-// 1/z to within about one ulp: hardware approximation plus one Newton step.
-__device__ __forceinline__ float rcp_nr(float z) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(z));
-  const float e = fmaf(-z, r, 1.f);
-  return fmaf(r, e, r);
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
