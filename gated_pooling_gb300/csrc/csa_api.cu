@@ -5,6 +5,8 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda.h>
+
 #include "csa_compressor.h"
 #include "csa_internal.h"
 
@@ -81,6 +83,43 @@ cudaError_t blocks_per_sm(int dev, const void* kernel, int threads, size_t smem,
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// 2-D tensor maps for the long-window kernel, encoded through the driver entry point the
+// runtime hands out (no link against the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// bf16 matrix [rows, cols] (row stride cols), boxes of [box_rows, box_cols] written to
+// shared memory with the 128-byte swizzle (box_cols * 2 must be 128).
+bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int cols, int box_cols,
+                     int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols),
+                              static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 csa_status_t check_sizes(int32_t S, int32_t ratio, int32_t coff, int32_t d, int64_t capacity,
                          int64_t out_rows) {
   if (S < 0 || ratio < 1 || d < 1 || capacity < 0 || out_rows < 0) return CSA_ERR_INVALID_VALUE;
@@ -105,10 +144,13 @@ csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t
   if (note(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
       cudaSuccess)
     return CSA_ERR_CUDA;
-  // Windows of <= 8 positions take the block-streaming kernel; longer ones the split kernel.
+  // Forward windows of <= 8 positions (or narrow rows) take the register-load kernel, other
+  // windows of <= 8 positions the block-streaming kernel, windows of 16..128 positions with
+  // d % 64 == 0 the tensor-copy kernel, everything else the split kernel.
   const size_t limit = static_cast<size_t>(optin) - 256;  // static shared memory headroom
   if (!(!bwd && plan_fwd_ldg(S, ratio, coff, d, limit, pl)) &&
-      !plan_stream(bwd, S, ratio, coff, d, limit, pl))
+      !plan_stream(bwd, S, ratio, coff, d, limit, pl) &&
+      !(encode_fn() != nullptr && plan_long(bwd, S, ratio, coff, d, limit, pl)))
     *pl = plan_shape(bwd, S, ratio, coff, d);
   *kernel = bwd ? bwd_kernel_for(*pl) : fwd_kernel_for(*pl);
   if (*kernel == nullptr) return CSA_ERR_UNSUPPORTED;
@@ -154,10 +196,26 @@ PoolParams base_params(const Plan& pl, const void* kv, const void* score, const 
   p.pre_off = pl.pre_off;
   p.ring_off = pl.ring_off;
   p.bar_off = pl.bar_off;
+  p.box_rows = pl.box_rows;
   return p;
 }
 
 csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t stream) {
+  if (pl.longk) {
+    // tensor maps over kv and score [capacity, C]; with no rows any aligned address will
+    // do (nothing is copied)
+    CUtensorMap mkv, msc;
+    const int sw = 4 * pl.Vs;  // 64 columns = one 128-byte swizzle row
+    const void* kv = p.kv != nullptr ? static_cast<const void*>(p.kv) : p.ape;
+    const void* sc = p.score != nullptr ? static_cast<const void*>(p.score) : p.ape;
+    if (!encode_bf16_map(&mkv, kv, p.capacity, p.C, sw, pl.box_rows) ||
+        !encode_bf16_map(&msc, sc, p.capacity, p.C, sw, pl.box_rows))
+      return CSA_ERR_CUDA;
+    void* args[] = {&p, &mkv, &msc};
+    cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
+                                          dim3(pl.threads), args, pl.smem, stream));
+    return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+  }
   void* args[] = {&p};
   cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
                                         dim3(pl.threads), args, pl.smem, stream));

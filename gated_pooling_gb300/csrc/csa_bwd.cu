@@ -1,11 +1,21 @@
 // csa_bwd.cu -- backward instantiations of the pooling kernel (4 columns per thread,
 // so that the per-thread dAPE sums fit in registers).
 #include "csa_internal.h"
+#include "csa_pool_long.cuh"
 #include "csa_pool_stream.cuh"
 
 namespace csa {
 
 PoolKernel bwd_kernel_for(const Plan& pl) {
+  if (pl.longk) {
+    switch (pl.pp) {
+      case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, true>);
+      case 2: return reinterpret_cast<PoolKernel>(pool_long_kernel<2, true>);
+      case 4: return reinterpret_cast<PoolKernel>(pool_long_kernel<4, true>);
+      case 8: return reinterpret_cast<PoolKernel>(pool_long_kernel<8, true>);
+      default: return nullptr;
+    }
+  }
   if (pl.tma) {
     const int r = pl.pp / pl.coff, coff = pl.coff;
     if (r == 1 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 1, 1, true>;

@@ -271,6 +271,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Global -> shared bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned),
 // counted against `bar`'s transaction count.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

@@ -1,11 +1,21 @@
 // csa_fwd.cu -- forward instantiations of the pooling kernel (8 columns per thread).
 #include "csa_internal.h"
+#include "csa_pool_long.cuh"
 #include "csa_fwd_ldg.cuh"
 #include "csa_pool_stream.cuh"
 
 namespace csa {
 
 PoolKernel fwd_kernel_for(const Plan& pl) {
+  if (pl.longk) {
+    switch (pl.pp) {
+      case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, false>);
+      case 2: return reinterpret_cast<PoolKernel>(pool_long_kernel<2, false>);
+      case 4: return reinterpret_cast<PoolKernel>(pool_long_kernel<4, false>);
+      case 8: return reinterpret_cast<PoolKernel>(pool_long_kernel<8, false>);
+      default: return nullptr;
+    }
+  }
   if (pl.ldg) {
     const int r = pl.pp / pl.coff, coff = pl.coff;
     if (r == 1 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 1, 1>;

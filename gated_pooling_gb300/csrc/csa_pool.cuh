@@ -69,6 +69,7 @@ struct PoolParams {
   int pre_off;      //   the block before the first row (left half),
   int ring_off;     //   the ring of stages,
   int bar_off;      //   the full/empty mbarriers
+  int box_rows;     // long windows: tokens per tensor box
 };
 
 // Zeroes rows [row0, row0+nrows) of dKV and dScore over this CTA's column slice (both
@@ -432,6 +433,8 @@ struct Plan {
   bool split = false;
   bool tma = false;  // block-streaming kernel (bulk copies) for windows of <= 8 positions
   bool ldg = false;  // forward through register loads (csa_fwd_ldg.cuh)
+  bool longk = false;  // long windows through 2-D tensor copies (csa_pool_long.cuh)
+  int box_rows = 0;    // long windows: tokens per tensor box
   int coff = 0;
   int threads = kThreads;
   int depth = 0, stage_bytes = 0, ape_off = 0, pre_off = 0, ring_off = 0, bar_off = 0;
@@ -572,6 +575,43 @@ inline bool plan_fwd_ldg(int S, int r, int coff, int d, size_t smem_limit, Plan*
   pl.smem = (size_t)pl.ape_off + (size_t)coff * r * d * 4;
   if (pl.smem > smem_limit) return false;
   pl.threads = CSA_LDG_THREADS;
+  *out = pl;
+  return true;
+}
+
+// Long-window geometry (csa_pool_long.cuh): W = coff*ratio in {16, 32, 64, 128} and d a
+// multiple of 64. A CTA slice is 64 columns per half (16 chunks of 4); a stage holds the
+// [W x 64] kv and score tiles (tile rows of 128 bytes, 1024-byte aligned for the 128-byte
+// swizzle; at coff=2 the own half starts at tile row ratio, a multiple of 8), the backward
+// adds the dout slice in a ring of its own. Tensor boxes are [ratio tokens x 64 columns].
+constexpr int kLongSliceCols = 64;  // columns per half in a long-window CTA slice
+
+inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
+  const int W = coff * r;
+  if (!(W == 16 || W == 32 || W == 64 || W == 128) || d % 64 != 0) return false;
+  Plan pl;
+  pl.longk = true;
+  pl.coff = coff;
+  pl.vec = 4;
+  pl.pp = W / 16;
+  pl.P = 16;
+  pl.V = d / 4;
+  pl.Vs = 16;
+  pl.K = d / 64;
+  pl.slots = 1;
+  pl.box_rows = r;
+  pl.sB_words = ((S + 1) + 3) & ~3;
+  const size_t ape_off = (size_t)pl.sB_words * 8;  // backward: ape of the slice, fp32
+  const size_t ring_off = ape_off + (bwd ? (size_t)W * kLongSliceCols * 4 : 0);
+  pl.stage_bytes = 2 * W * 128;
+  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 : 0) + 16;  // + 2 mbarriers
+  if (smem_limit < ring_off + 1024 + 2 * per_stage) return false;
+  const size_t depth = std::min<size_t>(16, (smem_limit - ring_off - 1024) / per_stage);
+  pl.depth = (int)depth;
+  pl.threads = kThreads + 32;
+  pl.ape_off = (int)ape_off;
+  pl.ring_off = (int)ring_off;
+  pl.smem = ring_off + 1024 + depth * per_stage;
   *out = pl;
   return true;
 }

@@ -1,0 +1,352 @@
+// csa_pool_long.cuh -- pooling kernel for long windows (W = coff*ratio in {16, 32, 64, 128};
+// e.g. the ratio=128 coff=1 family of "Megatron-LM PR #5984", commit "add dedicated
+// ratio=128 kernels"), forward and backward, for head dims that are multiples of 64.
+//
+// Same operation and zero ownership as pool_kernel (csa_pool.cuh). A CTA owns a slice of 64
+// columns per half and a contiguous range of output rows. For each row a producer warp
+// loads the slice's window with 2-D tensor-map bulk copies (TMA, 128-byte swizzle): one box
+// of [ratio tokens x 64 columns] per tensor per block half (at coff=2 the previous block at
+// the slice's first-half columns, the own block at its second-half columns), plus the dout
+// slice in the backward, into a ring of shared-memory stages completing on mbarriers.
+//
+// Consumers are 8 independent warps. Warp wi owns the 8 columns [8wi, 8wi+8) of the slice;
+// its lane (pg = lane % 16, ch = lane / 16) owns 4 of them and the window positions pg,
+// pg+16, pg+32, ... A column's max and its sums (sum e, sum e*kv) are reduced over the 16
+// position lanes with xor shuffles; the adds of a butterfly are commutative, so all 16
+// lanes end with the same bits and the result is the same on every run. Warps never wait
+// for each other: a stage is released once every consumer thread has arrived on its
+// `empty` barrier. The swizzle spreads the 16 rows a warp reads at once over all banks.
+// The ape values of a thread's (position, column) slots stay in registers in the forward
+// and in shared memory in the backward, whose registers hold the thread's dAPE sums instead
+// (the CTA's partial for those slots). All waits are bounded.
+#pragma once
+
+#include <cuda.h>
+
+#include "csa_pool.cuh"
+
+namespace csa {
+
+constexpr int kLongSlice = kLongSliceCols;  // one 128-byte tile row
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Byte offset of (tile row y, 16-byte chunk c) in a tile of 128-byte rows written with the
+// 128-byte swizzle (tile base on a 1024-byte boundary): the chunk is stored at c ^ (y mod 8).
+__device__ __forceinline__ int swz(int y, int c) { return y * 128 + ((c ^ (y & 7)) << 4); }
+
+template <int PP, bool BWD>
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    pool_long_kernel(const PoolParams p, const __grid_constant__ CUtensorMap tm_kv,
+                     const __grid_constant__ CUtensorMap tm_sc) {
+  constexpr int VEC = 4, NW = 2;
+  constexpr int W = 16 * PP;      // window positions
+  constexpr int kTile = W * 128;  // one tensor's window in a stage
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int warp_sums[32];
+  __shared__ int s_abort;
+  int* sB = reinterpret_cast<int*>(smem);
+  int* sCu = sB + p.sB_words;
+  // stages start on a 1024-byte boundary (the swizzle pattern); the plan reserves the slack
+  unsigned char* stages =
+      smem + p.ring_off + ((1024u - (smem_addr(smem + p.ring_off) & 1023u)) & 1023u);
+  unsigned char* gring = stages + static_cast<size_t>(p.depth) * p.stage_bytes;  // dout
+  uint64_t* full = reinterpret_cast<uint64_t*>(gring + (BWD ? p.depth * kLongSlice * 2 : 0));
+  uint64_t* empty = full + p.depth;
+
+  const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
+                                    warp_sums, sCu);
+  if (TC < 0) return;
+  if constexpr (BWD) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const int tid = threadIdx.x;
+  const int r = p.r, d = p.d, C = p.C;
+  const bool two = p.coff == 2;
+  const int col0 = blockIdx.x * kLongSlice;  // first column of the slice (in a half)
+  const int g = blockIdx.y;
+  const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
+  const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
+  const int nrows = o1 - o0;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int i = 0; i < p.depth; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kThreads);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (tid >= kThreads) {
+    // ------------------------------ producer ------------------------------------------
+    if (tid == kThreads) {
+      const uint64_t pol = l2_evict_first_policy();
+      int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
+      int j = 0;
+      for (; j < nrows; ++j) {
+        const int slot = j % p.depth;
+        if (j >= p.depth &&
+            !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>((j / p.depth - 1) & 1))) {
+          s_abort = 1;
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+        const int o = o0 + j;
+        s = advance_segment(sB, s, o);
+        const int b = o - sB[s];
+        const int base = sCu[s] + b * r;
+        const bool has_prev = two && b >= 1;
+        unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+        const int boxes = has_prev ? 2 : 1;
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(boxes * r * 128 * 2 +
+                                                                 (BWD ? kLongSlice * 2 : 0)));
+        if (has_prev) {  // previous block, first-half columns -> tile rows [0, r)
+          tma_load_2d(st, &tm_kv, col0, base - r, &full[slot], pol);
+          tma_load_2d(st + kTile, &tm_sc, col0, base - r, &full[slot], pol);
+        }
+        // own block -> tile rows [r, 2r) at coff=2 (second-half columns), [0, r) at coff=1
+        const int yo = two ? r * 128 : 0;
+        const int x = (two ? d : 0) + col0;
+        tma_load_2d(st + yo, &tm_kv, x, base, &full[slot], pol);
+        tma_load_2d(st + kTile + yo, &tm_sc, x, base, &full[slot], pol);
+        if constexpr (BWD)
+          bulk_load_hint(gring + slot * kLongSlice * 2,
+                         p.dout + static_cast<int64_t>(o) * d + col0, kLongSlice * 2,
+                         &full[slot], pol);
+      }
+      if (j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) {
+        if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
+        for (int k = max(0, j - p.depth); k < j; ++k)
+          mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1));
+      }
+    }
+    return;
+  }
+
+  // ------------------------------ consumers -------------------------------------------
+  const int lane = tid & 31;
+  const int wi = tid >> 5;         // 16-byte chunk of the slice row (8 columns)
+  const int pg = lane & 15;        // position lane
+  const int ch = lane >> 4;        // which 4 columns of the chunk
+  const int cl = wi * 8 + ch * 4;  // first column of this thread inside the slice
+
+  // ape of this thread's slots, scaled by log2 e: registers (forward) or shared memory
+  // [4-column group][position] (backward)
+  float ap[BWD ? 1 : PP][VEC];
+  float4* sAp = reinterpret_cast<float4*>(smem + p.ape_off) + (wi * 2 + ch) * W;
+#pragma unroll
+  for (int i = 0; i < PP; ++i) {
+    const int w = pg + 16 * i;
+    const bool prev = two && w < r;
+    const int arow = (two && !prev) ? w - r : w;
+    const int col = ((two && !prev) ? d : 0) + col0 + cl;
+    float4 a = __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(arow) * C + col));
+    a.x *= kLog2e;
+    a.y *= kLog2e;
+    a.z *= kLog2e;
+    a.w *= kLog2e;
+    if constexpr (BWD) {
+      sAp[w] = a;  // read back only by this thread
+    } else {
+      ap[i][0] = a.x;
+      ap[i][1] = a.y;
+      ap[i][2] = a.z;
+      ap[i][3] = a.w;
+    }
+  }
+  if constexpr (BWD) {  // short segments and rows outside [cu[0], cu[S]) of this slice
+    const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
+    const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
+    for (int s = s_lo; s < s_hi; ++s) {
+      const int a = sCu[s], b = sCu[s + 1];
+      if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, kLongSlice / VEC, tid, kThreads);
+    }
+    const int64_t c_first = sCu[0];
+    const int64_t c_last = sCu[p.S];
+    const int64_t npad = c_first + (p.capacity - c_last);
+    const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
+    const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
+    const int64_t h0 = min(q1, c_first);
+    if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, kLongSlice / VEC, tid, kThreads);
+    const int64_t t0 = max(q0, c_first), t1 = q1;
+    if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, kLongSlice / VEC, tid, kThreads);
+  }
+
+  float acc[PP][VEC];  // backward dAPE sums of this thread's slots
+#pragma unroll
+  for (int i = 0; i < PP; ++i)
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) acc[i][c] = 0.f;
+
+  int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
+  for (int j = 0; j < nrows; ++j) {
+    const int slot = j % p.depth;
+    const int o = o0 + j;
+    s = advance_segment(sB, s, o);
+    const int b = o - sB[s];
+    const int base = sCu[s] + b * r;
+    const bool has_prev = two && b >= 1;
+    const bool ok = mbar_wait_bounded(&full[slot], static_cast<uint32_t>((j / p.depth) & 1));
+    if (!__all_sync(0xFFFFFFFFu, ok) || *reinterpret_cast<volatile int*>(&s_abort)) {
+      s_abort = 1;
+      break;
+    }
+    const unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+
+    // x' = score*log2e + ape' at this thread's slots; invalid (first block, previous half)
+    // slots are -inf
+    float e[PP][VEC];
+    float m[VEC] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int i = 0; i < PP; ++i) {
+      const int w = pg + 16 * i;
+      if (two && w < r && !has_prev) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) e[i][c] = -INFINITY;
+        continue;
+      }
+      uint32_t sw[NW];
+      lds_words<NW>(sw, st + kTile + swz(w, wi) + ch * 8);
+      float4 a;
+      if constexpr (BWD) {
+        a = sAp[w];
+      } else {
+        a = make_float4(ap[i][0], ap[i][1], ap[i][2], ap[i][3]);
+      }
+      e[i][0] = fmaf(bf16_lo(sw[0]), kLog2e, a.x);
+      e[i][1] = fmaf(bf16_hi(sw[0]), kLog2e, a.y);
+      e[i][2] = fmaf(bf16_lo(sw[1]), kLog2e, a.z);
+      e[i][3] = fmaf(bf16_hi(sw[1]), kLog2e, a.w);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) m[c] = fmaxf(m[c], e[i][c]);
+    }
+#pragma unroll
+    for (int k = 1; k < 16; k <<= 1)
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) m[c] = fmaxf(m[c], __shfl_xor_sync(0xFFFFFFFFu, m[c], k));
+
+    // e = 2^(x' - m); two accumulation chains per column (one in the backward, which is
+    // short of registers)
+    constexpr int NCH = BWD ? 1 : 2;
+    float z[2][VEC], a[2][VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) z[0][c] = z[1][c] = a[0][c] = a[1][c] = 0.f;
+#pragma unroll
+    for (int i = 0; i < PP; ++i) {
+      const int w = pg + 16 * i;
+      if (two && w < r && !has_prev) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) e[i][c] = 0.f;
+        continue;
+      }
+      uint32_t kw[NW];
+      lds_words<NW>(kw, st + swz(w, wi) + ch * 8);
+      const float v[VEC] = {bf16_lo(kw[0]), bf16_hi(kw[0]), bf16_lo(kw[1]), bf16_hi(kw[1])};
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        e[i][c] = fast_exp2(e[i][c] - m[c]);
+        z[i % NCH][c] += e[i][c];
+        a[i % NCH][c] = fmaf(e[i][c], v[c], a[i % NCH][c]);
+      }
+    }
+    float Z[VEC], A[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      Z[c] = z[0][c] + z[1][c];
+      A[c] = a[0][c] + a[1][c];
+    }
+#pragma unroll
+    for (int k = 1; k < 16; k <<= 1)
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        Z[c] += __shfl_xor_sync(0xFFFFFFFFu, Z[c], k);
+        A[c] += __shfl_xor_sync(0xFFFFFFFFu, A[c], k);
+      }
+    float rz[VEC], oc[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      rz[c] = rcp_nr(Z[c]);
+      oc[c] = A[c] * rz[c];
+    }
+    if constexpr (!BWD) {
+      if (pg == 0) {
+        uint32_t ow[NW] = {pack_bf16x2(oc[0], oc[1]), pack_bf16x2(oc[2], oc[3])};
+        store_stream<NW>(p.out + static_cast<int64_t>(o) * d + col0 + cl, ow);
+      }
+    } else {
+      uint32_t gw[NW];
+      lds_words<NW>(gw, gring + slot * kLongSlice * 2 + cl * 2);
+      const float gv[VEC] = {bf16_lo(gw[0]), bf16_hi(gw[0]), bf16_lo(gw[1]), bf16_hi(gw[1])};
+      float qg[VEC];
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) qg[c] = rz[c] * gv[c];
+      // tile row w holds token base - r + w (coff=2) or base + w (coff=1)
+      const int tok0 = two ? base - r : base;
+#pragma unroll
+      for (int i = 0; i < PP; ++i) {
+        const int w = pg + 16 * i;
+        const bool prev = two && w < r;
+        if (prev && !has_prev) continue;
+        uint32_t kw[NW];
+        lds_words_fresh<NW>(kw, st + swz(w, wi) + ch * 8);
+        const float v[VEC] = {bf16_lo(kw[0]), bf16_hi(kw[0]), bf16_lo(kw[1]), bf16_hi(kw[1])};
+        float kk[VEC], t[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          kk[c] = e[i][c] * qg[c];
+          t[c] = kk[c] * (v[c] - oc[c]);
+          acc[i][c] += t[c];
+        }
+        const int64_t off = static_cast<int64_t>(tok0 + w) * C + (two && !prev ? d : 0) + col0 + cl;
+        const uint32_t dk[NW] = {pack_bf16x2(kk[0], kk[1]), pack_bf16x2(kk[2], kk[3])};
+        const uint32_t ds[NW] = {pack_bf16x2(t[0], t[1]), pack_bf16x2(t[2], t[3])};
+        store_stream<NW>(p.dkv + off, dk);
+        store_stream<NW>(p.dscore + off, ds);
+      }
+      const int n = sB[s + 1] - sB[s];
+      if (b == n - 1) {  // zeros owned by a segment's last block, spread over the lanes
+        const int64_t cz = col0 + cl;
+        if (two)  // the own block's first-half columns: no next block reads them
+          for (int k = pg; k < r; k += 16) {
+            const int64_t offz = static_cast<int64_t>(base + k) * C + cz;
+            store_zero<NW>(p.dkv + offz);
+            store_zero<NW>(p.dscore + offz);
+          }
+        const int ce = sCu[s + 1];
+        for (int t = sCu[s] + n * r + pg; t < ce; t += 16) {  // the segment's tail
+          const int64_t offz = static_cast<int64_t>(t) * C + cz;
+          store_zero<NW>(p.dkv + offz);
+          store_zero<NW>(p.dscore + offz);
+          if (two) {
+            store_zero<NW>(p.dkv + offz + d);
+            store_zero<NW>(p.dscore + offz + d);
+          }
+        }
+      }
+    }
+    mbar_arrive(&empty[slot]);
+  }
+
+  if constexpr (BWD) {  // this thread's dAPE slots are the CTA's partial for them
+    float* dst = p.partial + static_cast<int64_t>(g) * r * C;
+#pragma unroll
+    for (int i = 0; i < PP; ++i) {
+      const int w = pg + 16 * i;
+      const bool prev = two && w < r;
+      const int arow = (two && !prev) ? w - r : w;
+      const int col = ((two && !prev) ? d : 0) + col0 + cl;
+      *reinterpret_cast<float4*>(dst + static_cast<int64_t>(arow) * C + col) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+  }
+}
+
+}  // namespace csa

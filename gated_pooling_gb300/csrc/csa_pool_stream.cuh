@@ -26,10 +26,6 @@
 
 namespace csa {
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 template <int VEC, int NC, int R, int COFF, bool BWD>
 __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(const PoolParams p) {
   constexpr int NW = VEC / 2;  // 32-bit words (= column pairs) per chunk

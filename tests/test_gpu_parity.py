@@ -3,8 +3,9 @@
 Covers the five workload packs at full size (the launch configuration the bench
 times) and small packs that exercise every window shape the kernels specialise on:
 ragged packs, segments shorter than ratio, empty segments, tails, padding rows before
-cu_seqlens[0] and after cu_seqlens[S], coff 1 and 2, ratios 1..128, split windows,
-head dims whose chunk count does not fill a column slice, S = 0 and capacity 0.
+cu_seqlens[0] and after cu_seqlens[S], coff 1 and 2, ratios 1..128, split windows, the
+tensor-copy kernel's window sizes 16..128, head dims whose chunk count does not fill a
+column slice, S = 0 and capacity 0.
 The tolerance is the one tests/parity.py derives; the count of elements that needed
 its cancellation clause is capped.
 """
@@ -34,8 +35,22 @@ def small_packs():
         "r4c2_d264": ts.make_custom([33, 9], ratio=4, coff=2, d=264, pad_rows=2, seed=8),
         "r5c2_split_d16": ts.make_custom([31, 12, 4], ratio=5, coff=2, d=16, pad_rows=1, seed=9),
         "r16c2_split_d32": ts.make_custom([70, 33, 15], ratio=16, coff=2, d=32, pad_rows=2, seed=10),
-        "r128c1_split_d64": ts.make_custom([300, 129, 50], ratio=128, coff=1, d=64, pad_rows=7,
-                                           seed=11, score_scale=4.0),
+        "r128c1_d64": ts.make_custom([300, 129, 50], ratio=128, coff=1, d=64, pad_rows=7,
+                                     seed=11, score_scale=4.0),
+        # tensor-copy kernel for windows of 16..128 positions (d a multiple of 64): every
+        # positions-per-lane count, both coff, several column slices, tails and short
+        # segments, padding on both sides
+        "r8c2_d128": ts.make_custom([45, 7, 0, 64, 3], ratio=8, coff=2, d=128, pad_rows=5,
+                                    seed=20),
+        "r16c2_d64": ts.make_custom([90, 15, 49], ratio=16, coff=2, d=64, pad_rows=2, seed=21),
+        "r32c1_d192": ts.make_custom([100, 31, 64, 33], ratio=32, coff=1, d=192, pad_rows=6,
+                                     seed=22, score_scale=4.0),
+        "r32c2_d64": ts.make_custom([200, 40, 20], ratio=32, coff=2, d=64, pad_rows=1, seed=23),
+        "r64c1_d128": ts.make_custom([150, 64, 63], ratio=64, coff=1, d=128, pad_rows=4,
+                                     seed=24),
+        "r64c2_d64": ts.make_custom([260, 70, 10], ratio=64, coff=2, d=64, pad_rows=3, seed=25,
+                                    score_scale=4.0),
+        "r16c1_d64": ts.make_custom([50, 16, 5], ratio=16, coff=1, d=64, pad_rows=0, seed=26),
         "r128c2_split_d32": ts.make_custom([400, 128, 127], ratio=128, coff=2, d=32, pad_rows=3,
                                            seed=12),
         "all_short": ts.make_custom([1, 2, 3], ratio=4, coff=2, d=8, pad_rows=2, seed=13),
