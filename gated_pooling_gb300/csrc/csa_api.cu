@@ -204,14 +204,20 @@ csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t st
   if (pl.longk) {
     // tensor maps over kv and score [capacity, C]; with no rows any aligned address will
     // do (nothing is copied)
-    CUtensorMap mkv, msc;
+    // (the backward also stores dKV and dScore through maps; the forward gets copies of
+    // the input maps in those places and never uses them)
+    CUtensorMap mkv, msc, mdkv, mdsc;
     const int sw = 4 * pl.Vs;  // 64 columns = one 128-byte swizzle row
     const void* kv = p.kv != nullptr ? static_cast<const void*>(p.kv) : p.ape;
     const void* sc = p.score != nullptr ? static_cast<const void*>(p.score) : p.ape;
+    const void* dkv = p.dkv != nullptr ? static_cast<const void*>(p.dkv) : kv;
+    const void* dsc = p.dscore != nullptr ? static_cast<const void*>(p.dscore) : sc;
     if (!encode_bf16_map(&mkv, kv, p.capacity, p.C, sw, pl.box_rows) ||
-        !encode_bf16_map(&msc, sc, p.capacity, p.C, sw, pl.box_rows))
+        !encode_bf16_map(&msc, sc, p.capacity, p.C, sw, pl.box_rows) ||
+        !encode_bf16_map(&mdkv, dkv, p.capacity, p.C, sw, pl.box_rows) ||
+        !encode_bf16_map(&mdsc, dsc, p.capacity, p.C, sw, pl.box_rows))
       return CSA_ERR_CUDA;
-    void* args[] = {&p, &mkv, &msc};
+    void* args[] = {&p, &mkv, &msc, &mdkv, &mdsc};
     cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
                                           dim3(pl.threads), args, pl.smem, stream));
     return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;

@@ -9,10 +9,10 @@ namespace csa {
 PoolKernel bwd_kernel_for(const Plan& pl) {
   if (pl.longk) {
     switch (pl.pp) {
-      case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, true>);
-      case 2: return reinterpret_cast<PoolKernel>(pool_long_kernel<2, true>);
-      case 4: return reinterpret_cast<PoolKernel>(pool_long_kernel<4, true>);
-      case 8: return reinterpret_cast<PoolKernel>(pool_long_kernel<8, true>);
+      case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_BWD_GROUPS, true>);
+      case 2: return reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_BWD_GROUPS, true>);
+      case 4: return reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_BWD_GROUPS, true>);
+      case 8: return reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_BWD_GROUPS, true>);
       default: return nullptr;
     }
   }

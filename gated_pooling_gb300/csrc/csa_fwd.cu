@@ -9,10 +9,10 @@ namespace csa {
 PoolKernel fwd_kernel_for(const Plan& pl) {
   if (pl.longk) {
     switch (pl.pp) {
-      case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, false>);
-      case 2: return reinterpret_cast<PoolKernel>(pool_long_kernel<2, false>);
-      case 4: return reinterpret_cast<PoolKernel>(pool_long_kernel<4, false>);
-      case 8: return reinterpret_cast<PoolKernel>(pool_long_kernel<8, false>);
+      case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, false>);
+      case 2: return reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, false>);
+      case 4: return reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, false>);
+      case 8: return reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, false>);
       default: return nullptr;
     }
   }

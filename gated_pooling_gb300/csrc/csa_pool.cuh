@@ -583,8 +583,17 @@ inline bool plan_fwd_ldg(int S, int r, int coff, int d, size_t smem_limit, Plan*
 // multiple of 64. A CTA slice is 64 columns per half (16 chunks of 4); a stage holds the
 // [W x 64] kv and score tiles (tile rows of 128 bytes, 1024-byte aligned for the 128-byte
 // swizzle; at coff=2 the own half starts at tile row ratio, a multiple of 8), the backward
-// adds the dout slice in a ring of its own. Tensor boxes are [ratio tokens x 64 columns].
+// adds the dout slice in a ring of its own. Tensor boxes (loads, and the backward's
+// stores) are [ratio tokens x 64 columns].
 constexpr int kLongSliceCols = 64;  // columns per half in a long-window CTA slice
+
+// Consumer groups of 8 warps in the long-window kernel (csa_pool_long.cuh), per direction.
+#ifndef CSA_LONG_FWD_GROUPS
+#define CSA_LONG_FWD_GROUPS 3
+#endif
+#ifndef CSA_LONG_BWD_GROUPS
+#define CSA_LONG_BWD_GROUPS 2
+#endif
 
 inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
   const int W = coff * r;
@@ -601,14 +610,17 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit
   pl.slots = 1;
   pl.box_rows = r;
   pl.sB_words = ((S + 1) + 3) & ~3;
-  const size_t ape_off = (size_t)pl.sB_words * 8;  // backward: ape of the slice, fp32
-  const size_t ring_off = ape_off + (bwd ? (size_t)W * kLongSliceCols * 4 : 0);
+  const int ng = bwd ? CSA_LONG_BWD_GROUPS : CSA_LONG_FWD_GROUPS;
+  const bool ape_smem = bwd || ng > 1;  // else the forward keeps ape in registers
+  const size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
+  const size_t ring_off = ape_off + (ape_smem ? (size_t)16 * (W + 4) * 16 : 0);
   pl.stage_bytes = 2 * W * 128;
-  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 : 0) + 16;  // + 2 mbarriers
+  // + the dout slice and 3 mbarriers (backward), 2 mbarriers (forward)
+  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 + 24 : 16);
   if (smem_limit < ring_off + 1024 + 2 * per_stage) return false;
   const size_t depth = std::min<size_t>(16, (smem_limit - ring_off - 1024) / per_stage);
   pl.depth = (int)depth;
-  pl.threads = kThreads + 32;
+  pl.threads = ng * kThreads + (bwd ? 64 : 32);  // + producer warp (+ store warp)
   pl.ape_off = (int)ape_off;
   pl.ring_off = (int)ring_off;
   pl.smem = ring_off + 1024 + depth * per_stage;

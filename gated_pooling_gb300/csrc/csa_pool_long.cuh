@@ -7,18 +7,26 @@
 // loads the slice's window with 2-D tensor-map bulk copies (TMA, 128-byte swizzle): one box
 // of [ratio tokens x 64 columns] per tensor per block half (at coff=2 the previous block at
 // the slice's first-half columns, the own block at its second-half columns), plus the dout
-// slice in the backward, into a ring of shared-memory stages completing on mbarriers.
+// slice in the backward, into a ring of shared-memory stages completing on mbarriers. The
+// backward writes each slot's dKV and dScore over the kv and score values it has consumed in
+// the stage (every slot has exactly one reader and writer), and a store warp copies the
+// finished tiles out with tensor-map bulk stores, whole 128-byte tile rows at a time, before
+// it hands the stage back to the producer.
 //
-// Consumers are 8 independent warps. Warp wi owns the 8 columns [8wi, 8wi+8) of the slice;
-// its lane (pg = lane % 16, ch = lane / 16) owns 4 of them and the window positions pg,
-// pg+16, pg+32, ... A column's max and its sums (sum e, sum e*kv) are reduced over the 16
-// position lanes with xor shuffles; the adds of a butterfly are commutative, so all 16
-// lanes end with the same bits and the result is the same on every run. Warps never wait
-// for each other: a stage is released once every consumer thread has arrived on its
-// `empty` barrier. The swizzle spreads the 16 rows a warp reads at once over all banks.
-// The ape values of a thread's (position, column) slots stay in registers in the forward
-// and in shared memory in the backward, whose registers hold the thread's dAPE sums instead
-// (the CTA's partial for those slots). All waits are bounded.
+// Consumers are NG groups of 8 warps; group h takes the rows h, h+NG, ... of the CTA's
+// range (more groups keep more warps in flight where registers allow). Warp wi of a
+// group owns the 8 columns [8wi, 8wi+8) of the slice; its lane (pg = lane / 2,
+// ch = lane % 2) owns 4 of them and the window positions pg, pg+16, pg+32, ... A column's
+// max and its sums (sum e, sum e*kv) are reduced over the 16 position lanes with xor
+// shuffles; the adds of a butterfly are commutative, so all 16 lanes end with the same
+// bits and the result is the same on every run. Warps never wait for each other: a stage
+// is released once the 256 threads of its group have arrived on its `empty` barrier. The
+// swizzle puts the 8 rows that each half-warp reads at once on disjoint banks. The ape
+// values of a thread's slots are kept in registers (forward, one group) or in shared
+// memory; in the backward the registers hold the thread's dAPE sums, which the groups add
+// in a fixed order into the CTA's partial at the end. With two backward groups the
+// softmax terms are recomputed from the staged tile in each pass instead of being kept in
+// registers. All waits are bounded.
 #pragma once
 
 #include <cuda.h>
@@ -38,17 +46,48 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Shared -> global tensor-map bulk store of one box, tracked by the issuing thread's bulk
+// groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y,
+                                             const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   map),
+               "r"(x), "r"(y), "r"(smem_addr(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until every committed bulk group has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void sts_words2(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_addr(p)), "r"(a), "r"(b) : "memory");
+}
+
 // Byte offset of (tile row y, 16-byte chunk c) in a tile of 128-byte rows written with the
 // 128-byte swizzle (tile base on a 1024-byte boundary): the chunk is stored at c ^ (y mod 8).
 __device__ __forceinline__ int swz(int y, int c) { return y * 128 + ((c ^ (y & 7)) << 4); }
 
-template <int PP, bool BWD>
-__global__ void __launch_bounds__(kThreads + 32, 1)
+template <int PP, int NG, bool BWD>
+__global__ void __launch_bounds__(NG * kThreads + (BWD ? 64 : 32), 1)
     pool_long_kernel(const PoolParams p, const __grid_constant__ CUtensorMap tm_kv,
-                     const __grid_constant__ CUtensorMap tm_sc) {
+                     const __grid_constant__ CUtensorMap tm_sc,
+                     const __grid_constant__ CUtensorMap tm_dkv,
+                     const __grid_constant__ CUtensorMap tm_dsc) {
   constexpr int VEC = 4, NW = 2;
-  constexpr int W = 16 * PP;      // window positions
-  constexpr int kTile = W * 128;  // one tensor's window in a stage
+  constexpr int W = 16 * PP;          // window positions
+  constexpr int kTile = W * 128;      // one tensor's window in a stage
+  constexpr int NCT = NG * kThreads;  // consumer threads
+  static_assert(NG >= 1 && (!BWD || NG <= 2), "the dAPE combine handles two groups");
+  constexpr bool kApReg = !BWD && NG == 1;
+  constexpr bool kRecomp = BWD && NG > 1;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   __shared__ int s_abort;
@@ -60,6 +99,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   unsigned char* gring = stages + static_cast<size_t>(p.depth) * p.stage_bytes;  // dout
   uint64_t* full = reinterpret_cast<uint64_t*>(gring + (BWD ? p.depth * kLongSlice * 2 : 0));
   uint64_t* empty = full + p.depth;
+  uint64_t* done = empty + p.depth;  // backward: a group has written the stage's gradients
 
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
@@ -79,15 +119,53 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     s_abort = 0;
     for (int i = 0; i < p.depth; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kThreads);
+      mbar_init(&empty[i], BWD ? 1 : kThreads);  // backward: released by the store warp
+      if constexpr (BWD) mbar_init(&done[i], kThreads);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (tid >= kThreads) {
+  if (tid >= NCT) {
+    if constexpr (BWD) {
+      // ---------------------------- store warp ----------------------------------------
+      if (tid == NCT + 32) {
+        int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
+        bool bad = false;
+        for (int j = 0; j < nrows; ++j) {
+          const int slot = j % p.depth;
+          if (!mbar_wait_bounded(&done[slot], static_cast<uint32_t>((j / p.depth) & 1)) ||
+              *reinterpret_cast<volatile int*>(&s_abort)) {
+            bad = true;
+            break;
+          }
+          const int o = o0 + j;
+          s = advance_segment(sB, s, o);
+          const int base = sCu[s] + (o - sB[s]) * r;
+          const unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+          if (two && o > sB[s]) {  // previous block, first-half columns
+            tma_store_2d(&tm_dkv, col0, base - r, st);
+            tma_store_2d(&tm_dsc, col0, base - r, st + kTile);
+          }
+          const int yo = two ? r * 128 : 0;
+          const int x = (two ? d : 0) + col0;
+          tma_store_2d(&tm_dkv, x, base, st + yo);
+          tma_store_2d(&tm_dsc, x, base, st + kTile + yo);
+          bulk_commit();
+          if (j >= 1) {  // the previous row's tiles have been read: hand its stage back
+            bulk_wait_read<1>();
+            mbar_arrive(&empty[(j - 1) % p.depth]);
+          }
+        }
+        bulk_wait_all();
+        if (bad) {
+          s_abort = 1;
+          if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
+        }
+      }
+    }
     // ------------------------------ producer ------------------------------------------
-    if (tid == kThreads) {
+    if (tid == NCT) {
       const uint64_t pol = l2_evict_first_policy();
       int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
       int j = 0;
@@ -132,34 +210,38 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   }
 
   // ------------------------------ consumers -------------------------------------------
+  const int grp = tid / kThreads;
   const int lane = tid & 31;
-  const int wi = tid >> 5;         // 16-byte chunk of the slice row (8 columns)
-  const int pg = lane & 15;        // position lane
-  const int ch = lane >> 4;        // which 4 columns of the chunk
-  const int cl = wi * 8 + ch * 4;  // first column of this thread inside the slice
+  const int wi = (tid % kThreads) >> 5;  // 16-byte chunk of the slice row (8 columns)
+  const int pg = lane >> 1;              // position lane
+  const int ch = lane & 1;               // which 4 columns of the chunk
+  const int cl = wi * 8 + ch * 4;        // first column of this thread inside the slice
 
-  // ape of this thread's slots, scaled by log2 e: registers (forward) or shared memory
-  // [4-column group][position] (backward)
-  float ap[BWD ? 1 : PP][VEC];
-  float4* sAp = reinterpret_cast<float4*>(smem + p.ape_off) + (wi * 2 + ch) * W;
+  // ape of this thread's slots, scaled by log2 e: registers, or shared memory as
+  // [4-column group][position] float4 (written by group 0; groups W + 4 apart, so that the
+  // two column groups of a quarter-warp fall on different banks)
+  float ap[kApReg ? PP : 1][VEC];
+  float4* sAp = reinterpret_cast<float4*>(smem + p.ape_off) + (wi * 2 + ch) * (W + 4);
+  if (kApReg || grp == 0) {
 #pragma unroll
-  for (int i = 0; i < PP; ++i) {
-    const int w = pg + 16 * i;
-    const bool prev = two && w < r;
-    const int arow = (two && !prev) ? w - r : w;
-    const int col = ((two && !prev) ? d : 0) + col0 + cl;
-    float4 a = __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(arow) * C + col));
-    a.x *= kLog2e;
-    a.y *= kLog2e;
-    a.z *= kLog2e;
-    a.w *= kLog2e;
-    if constexpr (BWD) {
-      sAp[w] = a;  // read back only by this thread
-    } else {
-      ap[i][0] = a.x;
-      ap[i][1] = a.y;
-      ap[i][2] = a.z;
-      ap[i][3] = a.w;
+    for (int i = 0; i < PP; ++i) {
+      const int w = pg + 16 * i;
+      const bool prev = two && w < r;
+      const int arow = (two && !prev) ? w - r : w;
+      const int col = ((two && !prev) ? d : 0) + col0 + cl;
+      float4 a = __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(arow) * C + col));
+      a.x *= kLog2e;
+      a.y *= kLog2e;
+      a.z *= kLog2e;
+      a.w *= kLog2e;
+      if constexpr (kApReg) {
+        ap[i][0] = a.x;
+        ap[i][1] = a.y;
+        ap[i][2] = a.z;
+        ap[i][3] = a.w;
+      } else {
+        sAp[w] = a;
+      }
     }
   }
   if constexpr (BWD) {  // short segments and rows outside [cu[0], cu[S]) of this slice
@@ -167,7 +249,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
     for (int s = s_lo; s < s_hi; ++s) {
       const int a = sCu[s], b = sCu[s + 1];
-      if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, kLongSlice / VEC, tid, kThreads);
+      if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, kLongSlice / VEC, tid, NCT);
     }
     const int64_t c_first = sCu[0];
     const int64_t c_last = sCu[p.S];
@@ -175,19 +257,28 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
     const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
     const int64_t h0 = min(q1, c_first);
-    if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, kLongSlice / VEC, tid, kThreads);
+    if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, kLongSlice / VEC, tid, NCT);
     const int64_t t0 = max(q0, c_first), t1 = q1;
-    if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, kLongSlice / VEC, tid, kThreads);
+    if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, kLongSlice / VEC, tid, NCT);
   }
+  if constexpr (!kApReg) asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // ape staged
 
-  float acc[PP][VEC];  // backward dAPE sums of this thread's slots
+  auto ape_at = [&](const int i, const int w) -> float4 {
+    if constexpr (kApReg) {
+      return make_float4(ap[i][0], ap[i][1], ap[i][2], ap[i][3]);
+    } else {
+      return sAp[w];
+    }
+  };
+
+  float acc[BWD ? PP : 1][VEC];  // backward dAPE sums of this thread's slots
 #pragma unroll
-  for (int i = 0; i < PP; ++i)
+  for (int i = 0; i < (BWD ? PP : 1); ++i)
 #pragma unroll
     for (int c = 0; c < VEC; ++c) acc[i][c] = 0.f;
 
-  int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
-  for (int j = 0; j < nrows; ++j) {
+  int s = nrows > grp ? find_segment(sB, p.S, o0 + grp) : 0;
+  for (int j = grp; j < nrows; j += NG) {
     const int slot = j % p.depth;
     const int o = o0 + j;
     s = advance_segment(sB, s, o);
@@ -199,37 +290,36 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
       s_abort = 1;
       break;
     }
-    const unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+    unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
 
     // x' = score*log2e + ape' at this thread's slots; invalid (first block, previous half)
-    // slots are -inf
-    float e[PP][VEC];
+    // slots are skipped. With kRecomp the later passes read the slots again instead of
+    // keeping x' (and e) in registers.
+    auto x_at = [&](const int i, const int w, float (&x)[VEC]) {
+      uint32_t sw[NW];
+      lds_words<NW>(sw, st + kTile + swz(w, wi) + ch * 8);
+      const float4 a4 = ape_at(i, w);
+      x[0] = fmaf(bf16_lo(sw[0]), kLog2e, a4.x);
+      x[1] = fmaf(bf16_hi(sw[0]), kLog2e, a4.y);
+      x[2] = fmaf(bf16_lo(sw[1]), kLog2e, a4.z);
+      x[3] = fmaf(bf16_hi(sw[1]), kLog2e, a4.w);
+    };
+    float e[kRecomp ? 1 : PP][VEC];
     float m[VEC] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int i = 0; i < PP; ++i) {
       const int w = pg + 16 * i;
-      if (two && w < r && !has_prev) {
+      if (two && w < r && !has_prev) continue;
+      float x[VEC];
+      x_at(i, w, x);
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) e[i][c] = -INFINITY;
-        continue;
+      for (int c = 0; c < VEC; ++c) {
+        if constexpr (!kRecomp) e[i][c] = x[c];
+        m[c] = fmaxf(m[c], x[c]);
       }
-      uint32_t sw[NW];
-      lds_words<NW>(sw, st + kTile + swz(w, wi) + ch * 8);
-      float4 a;
-      if constexpr (BWD) {
-        a = sAp[w];
-      } else {
-        a = make_float4(ap[i][0], ap[i][1], ap[i][2], ap[i][3]);
-      }
-      e[i][0] = fmaf(bf16_lo(sw[0]), kLog2e, a.x);
-      e[i][1] = fmaf(bf16_hi(sw[0]), kLog2e, a.y);
-      e[i][2] = fmaf(bf16_lo(sw[1]), kLog2e, a.z);
-      e[i][3] = fmaf(bf16_hi(sw[1]), kLog2e, a.w);
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) m[c] = fmaxf(m[c], e[i][c]);
     }
 #pragma unroll
-    for (int k = 1; k < 16; k <<= 1)
+    for (int k = 2; k < 32; k <<= 1)
 #pragma unroll
       for (int c = 0; c < VEC; ++c) m[c] = fmaxf(m[c], __shfl_xor_sync(0xFFFFFFFFu, m[c], k));
 
@@ -242,19 +332,23 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 #pragma unroll
     for (int i = 0; i < PP; ++i) {
       const int w = pg + 16 * i;
-      if (two && w < r && !has_prev) {
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) e[i][c] = 0.f;
-        continue;
-      }
+      if (two && w < r && !has_prev) continue;
       uint32_t kw[NW];
       lds_words<NW>(kw, st + swz(w, wi) + ch * 8);
       const float v[VEC] = {bf16_lo(kw[0]), bf16_hi(kw[0]), bf16_lo(kw[1]), bf16_hi(kw[1])};
+      float x[VEC];
+      if constexpr (kRecomp) {
+        x_at(i, w, x);
+      } else {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) x[c] = e[i][c];
+      }
 #pragma unroll
       for (int c = 0; c < VEC; ++c) {
-        e[i][c] = fast_exp2(e[i][c] - m[c]);
-        z[i % NCH][c] += e[i][c];
-        a[i % NCH][c] = fmaf(e[i][c], v[c], a[i % NCH][c]);
+        const float ec = fast_exp2(x[c] - m[c]);
+        if constexpr (!kRecomp) e[i][c] = ec;
+        z[i % NCH][c] += ec;
+        a[i % NCH][c] = fmaf(ec, v[c], a[i % NCH][c]);
       }
     }
     float Z[VEC], A[VEC];
@@ -264,7 +358,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
       A[c] = a[0][c] + a[1][c];
     }
 #pragma unroll
-    for (int k = 1; k < 16; k <<= 1)
+    for (int k = 2; k < 32; k <<= 1)
 #pragma unroll
       for (int c = 0; c < VEC; ++c) {
         Z[c] += __shfl_xor_sync(0xFFFFFFFFu, Z[c], k);
@@ -288,8 +382,6 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
       float qg[VEC];
 #pragma unroll
       for (int c = 0; c < VEC; ++c) qg[c] = rz[c] * gv[c];
-      // tile row w holds token base - r + w (coff=2) or base + w (coff=1)
-      const int tok0 = two ? base - r : base;
 #pragma unroll
       for (int i = 0; i < PP; ++i) {
         const int w = pg + 16 * i;
@@ -298,18 +390,27 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         uint32_t kw[NW];
         lds_words_fresh<NW>(kw, st + swz(w, wi) + ch * 8);
         const float v[VEC] = {bf16_lo(kw[0]), bf16_hi(kw[0]), bf16_lo(kw[1]), bf16_hi(kw[1])};
+        float ei[VEC];
+        if constexpr (kRecomp) {
+          float x[VEC];
+          x_at(i, w, x);
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) ei[c] = fast_exp2(x[c] - m[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) ei[c] = e[i][c];
+        }
         float kk[VEC], t[VEC];
 #pragma unroll
         for (int c = 0; c < VEC; ++c) {
-          kk[c] = e[i][c] * qg[c];
+          kk[c] = ei[c] * qg[c];
           t[c] = kk[c] * (v[c] - oc[c]);
           acc[i][c] += t[c];
         }
-        const int64_t off = static_cast<int64_t>(tok0 + w) * C + (two && !prev ? d : 0) + col0 + cl;
-        const uint32_t dk[NW] = {pack_bf16x2(kk[0], kk[1]), pack_bf16x2(kk[2], kk[3])};
-        const uint32_t ds[NW] = {pack_bf16x2(t[0], t[1]), pack_bf16x2(t[2], t[3])};
-        store_stream<NW>(p.dkv + off, dk);
-        store_stream<NW>(p.dscore + off, ds);
+        // dKV and dScore replace the kv and score values of this slot in the stage
+        sts_words2(st + swz(w, wi) + ch * 8, pack_bf16x2(kk[0], kk[1]), pack_bf16x2(kk[2], kk[3]));
+        sts_words2(st + kTile + swz(w, wi) + ch * 8, pack_bf16x2(t[0], t[1]),
+                   pack_bf16x2(t[2], t[3]));
       }
       const int n = sB[s + 1] - sB[s];
       if (b == n - 1) {  // zeros owned by a segment's last block, spread over the lanes
@@ -332,10 +433,33 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         }
       }
     }
-    mbar_arrive(&empty[slot]);
+    if constexpr (BWD) {
+      fence_proxy_async_smem();  // the stage's new contents, to the bulk-store engine
+      mbar_arrive(&done[slot]);
+    } else {
+      mbar_arrive(&empty[slot]);
+    }
   }
 
-  if constexpr (BWD) {  // this thread's dAPE slots are the CTA's partial for them
+  if constexpr (BWD) {
+    // the CTA's dAPE partial for this thread's slots: group 0's sums, then group 1's
+    if constexpr (NG == 2) {
+      asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // ape no longer read
+      if (grp == 1)
+#pragma unroll
+        for (int i = 0; i < PP; ++i)
+          sAp[pg + 16 * i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
+      if (grp == 1) return;
+#pragma unroll
+      for (int i = 0; i < PP; ++i) {
+        const float4 o1v = sAp[pg + 16 * i];
+        acc[i][0] += o1v.x;
+        acc[i][1] += o1v.y;
+        acc[i][2] += o1v.z;
+        acc[i][3] += o1v.w;
+      }
+    }
     float* dst = p.partial + static_cast<int64_t>(g) * r * C;
 #pragma unroll
     for (int i = 0; i < PP; ++i) {
