@@ -39,7 +39,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---------------------------------------------------------------------------------
-// Vector IO: NW 32-bit words (NW = 2: 8 bytes, NW = 4: 16 bytes). Streaming loads are
+// Vector IO: NW 32-bit words (NW = 1, 2 or 4: 4, 8 or 16 bytes). Streaming loads are
 // read once (evict first, no L1 allocation); ape goes through the read-only path.
 // ---------------------------------------------------------------------------------
 template <int NW>
@@ -55,6 +55,10 @@ template <>
 __device__ __forceinline__ void load_stream<2>(uint32_t (&v)[2], const uint16_t* p) {
   asm volatile("ld.global.cs.v2.u32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "l"(p));
 }
+template <>
+__device__ __forceinline__ void load_stream<1>(uint32_t (&v)[1], const uint16_t* p) {
+  asm volatile("ld.global.cs.u32 %0, [%1];" : "=r"(v[0]) : "l"(p));
+}
 
 template <int NW>
 __device__ __forceinline__ void store_stream(uint16_t* p, const uint32_t (&v)[NW]);
@@ -68,6 +72,10 @@ __device__ __forceinline__ void store_stream<4>(uint16_t* p, const uint32_t (&v)
 template <>
 __device__ __forceinline__ void store_stream<2>(uint16_t* p, const uint32_t (&v)[2]) {
   asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v[0]), "r"(v[1]) : "memory");
+}
+template <>
+__device__ __forceinline__ void store_stream<1>(uint16_t* p, const uint32_t (&v)[1]) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v[0]) : "memory");
 }
 
 template <int NW>
@@ -296,13 +304,15 @@ __device__ __forceinline__ uint4 lds128_fresh(const void* p) {
   return v;
 }
 
-// NW 32-bit words from shared memory (16 or 8 bytes, aligned). The _fresh form is never
+// NW 32-bit words from shared memory (16, 8 or 4 bytes, aligned). The _fresh form is never
 // merged with an earlier load of the same address.
 template <int NW>
 __device__ __forceinline__ void lds_words(uint32_t (&v)[NW], const void* p) {
   if constexpr (NW == 4) {
     const uint4 t = *reinterpret_cast<const uint4*>(p);
     v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else if constexpr (NW == 1) {
+    v[0] = *reinterpret_cast<const uint32_t*>(p);
   } else {
     const uint2 t = *reinterpret_cast<const uint2*>(p);
     v[0] = t.x; v[1] = t.y;
@@ -314,6 +324,8 @@ __device__ __forceinline__ void lds_words_fresh(uint32_t (&v)[NW], const void* p
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
                  : "r"(smem_addr(p)));
+  } else if constexpr (NW == 1) {
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[0]) : "r"(smem_addr(p)));
   } else {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(smem_addr(p)));
   }

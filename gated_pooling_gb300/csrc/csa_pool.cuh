@@ -468,8 +468,13 @@ inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
 // Block-streaming kernel shape: columns per thread and consumer threads, per direction.
 // The backward keeps 4 columns per thread so that its per-thread dAPE sums and softmax
 // weights stay in registers.
-#ifndef CSA_STREAM_CTAS
-#define CSA_STREAM_CTAS 1  // CTAs per SM
+// CTAs per SM, per direction. Two forward CTAs per SM (two producers, each with half the
+// ring) read faster through bulk copies than one; the backward needs its registers.
+#ifndef CSA_STREAM_FWD_CTAS
+#define CSA_STREAM_FWD_CTAS 1
+#endif
+#ifndef CSA_STREAM_BWD_CTAS
+#define CSA_STREAM_BWD_CTAS 1
 #endif
 // Consumers plus one producer warp per CTA: 8 consumer warps + 1 producer put at most
 // three warps on an SM sub-partition, a 168-register budget per thread (no spills).
@@ -530,7 +535,8 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
   const size_t ring_off = (pre_off + (coff == 2 ? 2 * (size_t)r * C * 2 : 0) + 127) & ~(size_t)127;
   const size_t red = bwd ? (size_t)W * vec * nc * 4 : 0;
   // CTAs per SM share the SM's 228 KiB (1 KiB reserved per CTA)
-  smem_limit = std::min<size_t>(smem_limit, (228 * 1024) / CSA_STREAM_CTAS - 1024 - 256);
+  const int ctas = bwd ? CSA_STREAM_BWD_CTAS : CSA_STREAM_FWD_CTAS;
+  smem_limit = std::min<size_t>(smem_limit, (228 * 1024) / ctas - 1024 - 256);
   if (smem_limit <= ring_off + 64) return false;
   size_t depth = std::min<size_t>(64, (smem_limit - ring_off - 8) / (pl.stage_bytes + 16));
   while (depth >= 3 && ring_off + std::max(depth * pl.stage_bytes, red) + (2 * depth + 1) * 8 >
@@ -554,7 +560,12 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
 // Measured on GB300: register loads win for windows of <= 4 positions and for narrow rows
 // (d < 512), where the bulk-copy pipeline's start-up dominates; the block-streaming kernel
 // wins for 8-position windows of wide rows (the headline ratio=4 coff=2 d=512 pack).
-inline bool fwd_prefers_ldg(int r, int coff, int d) { return coff * r <= 4 || d < 512; }
+#ifndef CSA_FWD_LDG_MAX_WINDOW
+#define CSA_FWD_LDG_MAX_WINDOW 4
+#endif
+inline bool fwd_prefers_ldg(int r, int coff, int d) {
+  return coff * r <= CSA_FWD_LDG_MAX_WINDOW || d < 512;
+}
 
 inline bool plan_fwd_ldg(int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
   if (!CSA_FWD_LDG || !stream_window_supported(r, coff) || d % 4 != 0) return false;

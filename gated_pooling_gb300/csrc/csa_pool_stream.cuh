@@ -27,9 +27,11 @@
 namespace csa {
 
 template <int VEC, int NC, int R, int COFF, bool BWD>
-__global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(const PoolParams p) {
-  constexpr int NW = VEC / 2;  // 32-bit words (= column pairs) per chunk
-  constexpr int NH = VEC / 4;  // float4 of ape per chunk
+__global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREAM_FWD_CTAS)
+    pool_stream_kernel(const PoolParams p) {
+  constexpr int NW = VEC / 2;               // 32-bit words (= column pairs) per chunk
+  constexpr int AW = VEC >= 4 ? 4 : 2;      // ape values per shared-memory vector
+  constexpr int NA = VEC / AW;              // ape vectors per chunk
   constexpr int W = R * COFF;
   constexpr bool TWO = COFF == 2;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -37,7 +39,7 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
   __shared__ int s_abort;
   int* sB = reinterpret_cast<int*>(smem);                     // block prefix [S+1]
   int* sCu = sB + p.sB_words;                                  // cu_seqlens [S+1]
-  const float4* sA = reinterpret_cast<const float4*>(smem + p.ape_off);  // [W][NH][V]
+  const float* sA = reinterpret_cast<const float*>(smem + p.ape_off);  // [W][NA][V] x AW
   unsigned char* pre = smem + p.pre_off;  // block before the first row: kv, score [R][C]
   unsigned char* stages = smem + p.ring_off;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
@@ -97,10 +99,10 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
         }
       }
       int j = 0;
-      for (; j < nrows; ++j) {
-        const int slot = j % p.depth;
-        if (j >= p.depth &&
-            !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>((j / p.depth - 1) & 1))) {
+      int slot = 0;       // j % depth
+      uint32_t ph = 0;    // (j / depth) & 1
+      for (; j < nrows; ++j, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
+        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u)) {
           s_abort = 1;
           break;
         }
@@ -127,24 +129,32 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
   } else {
     // ------------------------------ consumers -----------------------------------------
     // While the first stages are in flight: stage ape (scaled by log2 e) as
-    // [w][h][chunk] float4 (a chunk's float4s are V apart) and, backward, write the
-    // zeros of segments shorter than ratio and of the padding rows of this row group.
+    // [w][h][chunk] vectors of AW values (a chunk's vectors are V apart) and, backward,
+    // write the zeros of segments shorter than ratio and of the padding rows of this row
+    // group.
     {
-      float4* dstA = reinterpret_cast<float4*>(smem + p.ape_off);
-      for (int it = tid; it < W * NH * V; it += NC) {
-        const int w = it / (NH * V);
-        const int h = (it / V) % NH;
+      float* dstA = reinterpret_cast<float*>(smem + p.ape_off);
+      for (int it = tid; it < W * NA * V; it += NC) {
+        const int w = it / (NA * V);
+        const int h = (it / V) % NA;
         const int ch = it % V;
         const bool prev = TWO && w < R;
         const int arow = (TWO && !prev) ? w - R : w;
-        const int col = ((TWO && !prev) ? d : 0) + ch * VEC + 4 * h;
-        float4 a =
-            __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(arow) * C + col));
-        a.x *= kLog2e;
-        a.y *= kLog2e;
-        a.z *= kLog2e;
-        a.w *= kLog2e;
-        dstA[it] = a;
+        const int col = ((TWO && !prev) ? d : 0) + ch * VEC + AW * h;
+        const float* src = p.ape + static_cast<int64_t>(arow) * C + col;
+        if constexpr (AW == 4) {
+          float4 a = __ldg(reinterpret_cast<const float4*>(src));
+          a.x *= kLog2e;
+          a.y *= kLog2e;
+          a.z *= kLog2e;
+          a.w *= kLog2e;
+          reinterpret_cast<float4*>(dstA)[it] = a;
+        } else {
+          float2 a = __ldg(reinterpret_cast<const float2*>(src));
+          a.x *= kLog2e;
+          a.y *= kLog2e;
+          reinterpret_cast<float2*>(dstA)[it] = a;
+        }
       }
     }
     if constexpr (BWD) {
@@ -173,8 +183,13 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
     const uint64_t kL2 = f2_pack(kLog2e, kLog2e);
     if (rs < p.slots && rs < nrows) {
       int s = find_segment(sB, p.S, o0 + rs);
+      // stage of row j and its phase parity, advanced by `slots` rows per iteration
+      // (slots < depth), and the same for row j - 1
+      int slot = rs;  // rs < slots < depth
+      uint32_t ph = 0;
       for (int j = rs; j < nrows; j += p.slots) {
-        const int slot = j % p.depth;
+        const int pslot = slot == 0 ? p.depth - 1 : slot - 1;
+        const uint32_t pph = slot == 0 ? ph ^ 1u : ph;
         const int o = o0 + j;
         s = advance_segment(sB, s, o);
         const int b = o - sB[s];
@@ -182,7 +197,7 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
         const int cs = sCu[s];
         const int base = cs + b * R;
         const bool has_prev = TWO && b >= 1;
-        bool ok = mbar_wait_bounded(&full[slot], static_cast<uint32_t>((j / p.depth) & 1));
+        bool ok = mbar_wait_bounded(&full[slot], ph);
         // kv chunk of the own block's first token; score sits kv_bytes further, rows are C2
         // bytes apart. The previous block (coff=2) uses the same layout (its own stage, or
         // the block fetched before the first row).
@@ -195,8 +210,7 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
             ok = ok && mbar_wait_bounded(pre_bar, 0);
             prev_kv = pre + c0 * 2;
           } else {
-            const int pslot = (j - 1) % p.depth;
-            ok = ok && mbar_wait_bounded(&full[pslot], static_cast<uint32_t>(((j - 1) / p.depth) & 1));
+            ok = ok && mbar_wait_bounded(&full[pslot], pph);
             prev_kv = stages + static_cast<size_t>(pslot) * p.stage_bytes + c0 * 2;
           }
         }
@@ -212,10 +226,15 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
           lds_words<NW>(sw, kvp + kv_bytes);
           uint64_t a2[NW];
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            const float4 a = sA[(i * NH + h) * V + vl];
-            a2[2 * h] = f2_pack(a.x, a.y);
-            a2[2 * h + 1] = f2_pack(a.z, a.w);
+          for (int h = 0; h < NA; ++h) {
+            if constexpr (AW == 4) {
+              const float4 a = reinterpret_cast<const float4*>(sA)[(i * NA + h) * V + vl];
+              a2[2 * h] = f2_pack(a.x, a.y);
+              a2[2 * h + 1] = f2_pack(a.z, a.w);
+            } else {
+              const float2 a = reinterpret_cast<const float2*>(sA)[(i * NA + h) * V + vl];
+              a2[h] = f2_pack(a.x, a.y);
+            }
           }
 #pragma unroll
           for (int q = 0; q < NW; ++q) x[i][q] = f2_fma(bf2_to_f2(sw[q]), kL2, a2[q]);
@@ -354,7 +373,12 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
         }
         // release the own stage and (coff=2) the previous one, which row o-1 also read
         mbar_arrive(&empty[slot]);
-        if (TWO && j >= 1) mbar_arrive(&empty[(j - 1) % p.depth]);
+        if (TWO && j >= 1) mbar_arrive(&empty[pslot]);
+        slot += p.slots;
+        if (slot >= p.depth) {
+          slot -= p.depth;
+          ph ^= 1u;
+        }
       }
     }
   }
@@ -389,9 +413,13 @@ __global__ void __launch_bounds__(NC + 32, CSA_STREAM_CTAS) pool_stream_kernel(c
         const int col = ((TWO && !prev) ? d : 0) + c0;
         float* q = dst + static_cast<int64_t>(arow) * C + col;
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
-          *reinterpret_cast<float4*>(q + 4 * h) =
-              make_float4(sum[4 * h], sum[4 * h + 1], sum[4 * h + 2], sum[4 * h + 3]);
+        for (int h = 0; h < NA; ++h) {
+          if constexpr (AW == 4)
+            *reinterpret_cast<float4*>(q + 4 * h) =
+                make_float4(sum[4 * h], sum[4 * h + 1], sum[4 * h + 2], sum[4 * h + 3]);
+          else
+            *reinterpret_cast<float2*>(q + 2 * h) = make_float2(sum[2 * h], sum[2 * h + 1]);
+        }
       }
     }
   }
