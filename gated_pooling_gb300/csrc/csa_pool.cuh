@@ -630,6 +630,7 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit
   const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 + 24 : 16);
   if (smem_limit < ring_off + 1024 + 2 * per_stage) return false;
   const size_t depth = std::min<size_t>(16, (smem_limit - ring_off - 1024) / per_stage);
+  if (depth <= (size_t)ng) return false;  // every consumer group needs a stage of its own
   pl.depth = (int)depth;
   pl.threads = ng * kThreads + (bwd ? 64 : 32);  // + producer warp (+ store warp)
   pl.ape_off = (int)ape_off;

@@ -132,9 +132,11 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 64 : 32), 1)
       if (tid == NCT + 32) {
         int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
         bool bad = false;
-        for (int j = 0; j < nrows; ++j) {
-          const int slot = j % p.depth;
-          if (!mbar_wait_bounded(&done[slot], static_cast<uint32_t>((j / p.depth) & 1)) ||
+        int slot = 0, pslot = 0;  // stages of rows j and j - 1
+        uint32_t ph = 0;          // (j / depth) & 1
+        for (int j = 0; j < nrows;
+             ++j, pslot = slot, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
+          if (!mbar_wait_bounded(&done[slot], ph) ||
               *reinterpret_cast<volatile int*>(&s_abort)) {
             bad = true;
             break;
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 64 : 32), 1)
           bulk_commit();
           if (j >= 1) {  // the previous row's tiles have been read: hand its stage back
             bulk_wait_read<1>();
-            mbar_arrive(&empty[(j - 1) % p.depth]);
+            mbar_arrive(&empty[pslot]);
           }
         }
         bulk_wait_all();
@@ -169,10 +171,10 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 64 : 32), 1)
       const uint64_t pol = l2_evict_first_policy();
       int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
       int j = 0;
-      for (; j < nrows; ++j) {
-        const int slot = j % p.depth;
-        if (j >= p.depth &&
-            !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>((j / p.depth - 1) & 1))) {
+      int slot = 0;     // j % depth
+      uint32_t ph = 0;  // (j / depth) & 1
+      for (; j < nrows; ++j, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
+        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u)) {
           s_abort = 1;
           break;
         }
@@ -278,14 +280,18 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 64 : 32), 1)
     for (int c = 0; c < VEC; ++c) acc[i][c] = 0.f;
 
   int s = nrows > grp ? find_segment(sB, p.S, o0 + grp) : 0;
-  for (int j = grp; j < nrows; j += NG) {
-    const int slot = j % p.depth;
+  // stage of row j and its phase parity, advanced by NG rows per iteration (NG < depth):
+  // the new slot is below NG exactly when it wrapped
+  int slot = grp;
+  uint32_t ph = 0;
+  for (int j = grp; j < nrows;
+       j += NG, slot = slot + NG >= p.depth ? slot + NG - p.depth : slot + NG, ph ^= slot < NG) {
     const int o = o0 + j;
     s = advance_segment(sB, s, o);
     const int b = o - sB[s];
     const int base = sCu[s] + b * r;
     const bool has_prev = two && b >= 1;
-    const bool ok = mbar_wait_bounded(&full[slot], static_cast<uint32_t>((j / p.depth) & 1));
+    const bool ok = mbar_wait_bounded(&full[slot], ph);
     if (!__all_sync(0xFFFFFFFFu, ok) || *reinterpret_cast<volatile int*>(&s_abort)) {
       s_abort = 1;
       break;

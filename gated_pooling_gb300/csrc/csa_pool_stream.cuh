@@ -22,6 +22,8 @@
 // in registers; every wait is bounded.
 #pragma once
 
+#include <type_traits>
+
 #include "csa_pool.cuh"
 
 namespace csa {
@@ -46,30 +48,42 @@ __global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREA
   uint64_t* empty = full + p.depth;
   uint64_t* pre_bar = empty + p.depth;
 
+  const int tid = threadIdx.x;
+  const int d = p.d, C = p.C, V = p.V;
+
+  using ApeVec = typename std::conditional<AW == 4, float4, float2>::type;
+  auto ape_src = [&](const int it) {
+    const int w = it / (NA * V);
+    const int h = (it / V) % NA;
+    const int ch = it % V;
+    const bool prev = TWO && w < R;
+    const int arow = (TWO && !prev) ? w - R : w;
+    const int col = ((TWO && !prev) ? d : 0) + ch * VEC + AW * h;
+    return reinterpret_cast<const ApeVec*>(p.ape + static_cast<int64_t>(arow) * C + col);
+  };
+  // mbarriers, one per thread, before the map is read: their set-up does not depend on it.
+  // The CTA-scope proxy fence makes them visible to the bulk-copy engine; the barriers
+  // inside the block prefix make them visible to the other threads.
+  if (tid < 2 * p.depth + 1) {
+    if (tid < p.depth) mbar_init(&full[tid], 1);
+    else if (tid < 2 * p.depth) mbar_init(&empty[tid - p.depth], COFF * V);
+    else mbar_init(pre_bar, 1);
+    fence_proxy_async_smem();
+  }
+  if (tid == 0) s_abort = 0;
+
+  // (the block prefix ends with a barrier: the mbarriers are ready after it)
   const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
   if (TC < 0) return;
   if constexpr (BWD) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  const int tid = threadIdx.x;
-  const int d = p.d, C = p.C, V = p.V;
   const int g = blockIdx.y;
   const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
   const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
   const int nrows = o1 - o0;
   const int kv_bytes = R * C * 2;  // one block of kv (or score), full width
   const int stage_g = 2 * kv_bytes;
-
-  if (tid == 0) {
-    s_abort = 0;
-    for (int i = 0; i < p.depth; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], COFF * V);
-    }
-    mbar_init(pre_bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();  // barriers ready: the producer starts streaming right away
 
   // does row o0 read a previous block (coff = 2 and not a segment's first block)?
   bool need_pre = false;
@@ -86,18 +100,23 @@ __global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREA
 
   if (tid >= NC) {
     // ------------------------------ producer ------------------------------------------
-    if (tid == NC) {
-      const uint64_t pol = l2_evict_first_policy();
-      int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
-      if (need_pre) {
-        const int base = sCu[s] + (o0 - sB[s] - 1) * R;
-        mbar_arrive_expect_tx(pre_bar, static_cast<uint32_t>(2 * R * d * 2));
-        for (int w = 0; w < R; ++w) {
-          const int64_t off = static_cast<int64_t>(base + w) * C;
-          bulk_load_hint(pre + w * C * 2, p.kv + off, d * 2, pre_bar, pol);
-          bulk_load_hint(pre + kv_bytes + w * C * 2, p.score + off, d * 2, pre_bar, pol);
-        }
+    // the producer warp's lanes issue the previous block's 2*R row copies together; lane 0
+    // then streams the stages
+    const int lane = tid - NC;
+    const uint64_t pol = l2_evict_first_policy();
+    int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
+    if (need_pre) {
+      if (lane == 0) mbar_arrive_expect_tx(pre_bar, static_cast<uint32_t>(2 * R * d * 2));
+      __syncwarp();
+      if (lane < 2 * R) {
+        const int w = lane % R;
+        const bool sc = lane >= R;
+        const int64_t off = static_cast<int64_t>(sCu[s] + (o0 - sB[s] - 1) * R + w) * C;
+        bulk_load_hint(pre + (sc ? kv_bytes : 0) + w * C * 2, (sc ? p.score : p.kv) + off,
+                       d * 2, pre_bar, pol);
       }
+    }
+    if (lane == 0) {
       int j = 0;
       int slot = 0;       // j % depth
       uint32_t ph = 0;    // (j / depth) & 1
@@ -133,29 +152,17 @@ __global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREA
     // write the zeros of segments shorter than ratio and of the padding rows of this row
     // group.
     {
-      float* dstA = reinterpret_cast<float*>(smem + p.ape_off);
-      for (int it = tid; it < W * NA * V; it += NC) {
-        const int w = it / (NA * V);
-        const int h = (it / V) % NA;
-        const int ch = it % V;
-        const bool prev = TWO && w < R;
-        const int arow = (TWO && !prev) ? w - R : w;
-        const int col = ((TWO && !prev) ? d : 0) + ch * VEC + AW * h;
-        const float* src = p.ape + static_cast<int64_t>(arow) * C + col;
+      ApeVec* dstA = reinterpret_cast<ApeVec*>(smem + p.ape_off);
+      auto put = [&](const int it, ApeVec a) {
+        a.x *= kLog2e;
+        a.y *= kLog2e;
         if constexpr (AW == 4) {
-          float4 a = __ldg(reinterpret_cast<const float4*>(src));
-          a.x *= kLog2e;
-          a.y *= kLog2e;
           a.z *= kLog2e;
           a.w *= kLog2e;
-          reinterpret_cast<float4*>(dstA)[it] = a;
-        } else {
-          float2 a = __ldg(reinterpret_cast<const float2*>(src));
-          a.x *= kLog2e;
-          a.y *= kLog2e;
-          reinterpret_cast<float2*>(dstA)[it] = a;
         }
-      }
+        dstA[it] = a;
+      };
+      for (int it = tid; it < W * NA * V; it += NC) put(it, __ldg(ape_src(it)));
     }
     if constexpr (BWD) {
       const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
