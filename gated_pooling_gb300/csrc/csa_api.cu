@@ -237,16 +237,19 @@ __device__ __forceinline__ void neumaier_add(float& s, float& c, float x) {
 }
 
 // dAPE = (accumulate ? dAPE : 0) + sum over row groups g = 0..R-1 of partial[g]. A block
-// covers 32 entries with 32 warps; warp k adds the contiguous row-group range
-// [k*R/32, (k+1)*R/32) (a few partials: their loads overlap) with compensated fp32 sums,
-// then warp 0 adds the 32 range sums in order. The result is the same bits on every
-// run. Launched as a programmatic dependent of the pooling kernel: it may start early
-// and waits for that grid's results.
+// covers 32 entries with SPLIT warps; warp k adds the contiguous row-group range
+// [k*R/SPLIT, (k+1)*R/SPLIT) (loaded kReduceBatch at a time, so the loads overlap) with
+// compensated fp32 sums, then warp 0 adds the range sums in order. SPLIT follows R (about
+// five partials per warp), so that few threads idle. The result is the same bits on every
+// run. Launched as a programmatic dependent of the pooling kernel: it may start early and
+// waits for that grid's results.
 constexpr int kReduceCols = 32;
-constexpr int kReduceSplit = 32;
-__global__ void __launch_bounds__(kReduceCols * kReduceSplit)
+constexpr int kReduceBatch = 12;  // partials a thread has in flight at once
+template <int SPLIT>
+__global__ void __launch_bounds__(kReduceCols * SPLIT)
     dape_reduce_kernel(const float* __restrict__ partial, int R, int n, float* __restrict__ dape,
                        int accumulate) {
+  constexpr int kReduceSplit = SPLIT;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float s_sum[kReduceSplit][kReduceCols];
   __shared__ float s_cmp[kReduceSplit][kReduceCols];
@@ -256,8 +259,18 @@ __global__ void __launch_bounds__(kReduceCols * kReduceSplit)
   const int g_lo = static_cast<int>(static_cast<int64_t>(k) * R / kReduceSplit);
   const int g_hi = static_cast<int>(static_cast<int64_t>(k + 1) * R / kReduceSplit);
   float s = 0.f, c = 0.f;
-  if (e < n)
-    for (int g = g_lo; g < g_hi; ++g) neumaier_add(s, c, __ldg(partial + static_cast<int64_t>(g) * n + e));
+  if (e < n) {
+    // kReduceBatch partials in flight at a time, added in ascending g
+    for (int g0 = g_lo; g0 < g_hi; g0 += kReduceBatch) {
+      float v[kReduceBatch];
+#pragma unroll
+      for (int u = 0; u < kReduceBatch; ++u)
+        v[u] = g0 + u < g_hi ? __ldg(partial + static_cast<int64_t>(g0 + u) * n + e) : 0.f;
+#pragma unroll
+      for (int u = 0; u < kReduceBatch; ++u)
+        if (g0 + u < g_hi) neumaier_add(s, c, v[u]);
+    }
+  }
   s_sum[k][lane] = s;
   s_cmp[k][lane] = c;
   __syncthreads();
@@ -396,14 +409,23 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
+  // warps per block: the power of two nearest above R/5, at most 32
+  int split = 1;
+  while (split < 32 && split * 5 < R) split *= 2;
+  const void* rk = split == 1    ? reinterpret_cast<const void*>(dape_reduce_kernel<1>)
+                   : split == 2  ? reinterpret_cast<const void*>(dape_reduce_kernel<2>)
+                   : split == 4  ? reinterpret_cast<const void*>(dape_reduce_kernel<4>)
+                   : split == 8  ? reinterpret_cast<const void*>(dape_reduce_kernel<8>)
+                   : split == 16 ? reinterpret_cast<const void*>(dape_reduce_kernel<16>)
+                                 : reinterpret_cast<const void*>(dape_reduce_kernel<32>);
   cfg.gridDim = dim3((n + kReduceCols - 1) / kReduceCols);
-  cfg.blockDim = dim3(kReduceCols * kReduceSplit);
+  cfg.blockDim = dim3(kReduceCols * split);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e =
-      note(cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(dape_reduce_kernel), rargs));
+      note(cudaLaunchKernelExC(&cfg, rk, rargs));
   return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
 
