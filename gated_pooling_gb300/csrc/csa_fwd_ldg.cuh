@@ -7,8 +7,9 @@
 // enough of them in flight, so this variant keeps everything in registers: each thread
 // owns one chunk of 4 columns of a row (both halves at coff=2) and loads, per row, the
 // 2*W 8-byte pieces of its window (kv and score) itself. The loads of the thread's next
-// row are issued before the current row is computed (a register double buffer), so every
-// thread always has a row in flight. CTAs are persistent (one per SM, or two) and own a
+// PF rows are in flight while a row is computed (a ring of PF + 1 register buffers; PF is
+// larger for shorter windows, whose buffers are smaller), so that enough bytes are in
+// flight to cover the memory latency. CTAs are persistent (one per SM, or two) and own a
 // contiguous range of rows, split over their row slots.
 #pragma once
 
@@ -84,20 +85,27 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
     }
   };
 
-  uint32_t kv[W][NW], sc[W][NW];
-  bool hp = false;
-  fetch(rs, kv, sc, hp);
-  for (int j = rs; j < nrows; j += p.slots) {
-    uint32_t kvn[W][NW], scn[W][NW];
-    bool hpn = false;
-    const bool more = j + p.slots < nrows;
-    if (more) fetch(j + p.slots, kvn, scn, hpn);
+  // rows in flight ahead of the one being computed
+#ifndef CSA_LDG_PF4
+#define CSA_LDG_PF4 2  // rows ahead for windows of 4 positions
+#endif
+  constexpr int PF = W >= 8 ? 1 : (W >= 4 ? CSA_LDG_PF4 : 3);
+  uint32_t kv[PF + 1][W][NW], sc[PF + 1][W][NW];
+  bool hp[PF + 1];
+#pragma unroll
+  for (int k = 0; k < PF; ++k) {
+    hp[k] = false;
+    if (rs + k * p.slots < nrows) fetch(rs + k * p.slots, kv[k], sc[k], hp[k]);
+  }
+  hp[PF] = false;
 
+  auto compute = [&](const int j, const uint32_t (&kvb)[W][NW], const uint32_t (&scb)[W][NW],
+                     const bool has_prev) {
     uint64_t x[W][NW];
 #pragma unroll
     for (int i = 0; i < W; ++i) {
       const bool prev = TWO && i < R;
-      if (prev && !hp) {
+      if (prev && !has_prev) {
 #pragma unroll
         for (int q = 0; q < NW; ++q) x[i][q] = f2_pack(-INFINITY, -INFINITY);
         continue;
@@ -105,7 +113,7 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
       const float4 a = sA[i * V + vl];
       const uint64_t a2[2] = {f2_pack(a.x, a.y), f2_pack(a.z, a.w)};
 #pragma unroll
-      for (int q = 0; q < NW; ++q) x[i][q] = f2_fma(bf2_to_f2(sc[i][q]), kL2, a2[q]);
+      for (int q = 0; q < NW; ++q) x[i][q] = f2_fma(bf2_to_f2(scb[i][q]), kL2, a2[q]);
     }
     uint64_t nm[NW];
 #pragma unroll
@@ -128,13 +136,13 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
 #pragma unroll
     for (int i = 0; i < W; ++i) {
       const bool prev = TWO && i < R;
-      if (prev && !hp) continue;
+      if (prev && !has_prev) continue;
 #pragma unroll
       for (int q = 0; q < NW; ++q) {
         const uint64_t dd = f2_add(x[i][q], nm[q]);
         const uint64_t e2 = f2_pack(fast_exp2(f2_lo(dd)), fast_exp2(f2_hi(dd)));
         zz[i & 1][q] = f2_add(zz[i & 1][q], e2);
-        AA[i & 1][q] = f2_fma(e2, bf2_to_f2(kv[i][q]), AA[i & 1][q]);
+        AA[i & 1][q] = f2_fma(e2, bf2_to_f2(kvb[i][q]), AA[i & 1][q]);
       }
     }
     uint32_t ow[NW];
@@ -145,16 +153,21 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
       ow[q] = f2_to_bf2(f2_mul(A, f2_pack(rcp_nr(f2_lo(z)), rcp_nr(f2_hi(z)))));
     }
     store_stream<NW>(p.out + static_cast<int64_t>(o0 + j) * d + c0, ow);
+  };
 
-    if (more) {
+  // step b computes buffer b and refills buffer (b + PF) mod (PF + 1) with the row PF
+  // slots ahead (the buffer the previous step consumed); the unrolled steps keep every
+  // buffer index a constant
+  for (int j = rs; j < nrows;) {
 #pragma unroll
-      for (int i = 0; i < W; ++i)
-#pragma unroll
-        for (int q = 0; q < NW; ++q) {
-          kv[i][q] = kvn[i][q];
-          sc[i][q] = scn[i][q];
-        }
-      hp = hpn;
+    for (int b = 0; b <= PF; ++b) {
+      if (j < nrows) {
+        const int jn = j + PF * p.slots;
+        const int bn = (b + PF) % (PF + 1);
+        if (jn < nrows) fetch(jn, kv[bn], sc[bn], hp[bn]);
+        compute(j, kv[b], sc[b], hp[b]);
+        j += p.slots;
+      }
     }
   }
   (void)NH;

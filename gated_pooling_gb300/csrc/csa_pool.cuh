@@ -563,8 +563,11 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
 #ifndef CSA_FWD_LDG_MAX_WINDOW
 #define CSA_FWD_LDG_MAX_WINDOW 4
 #endif
+#ifndef CSA_FWD_LDG_BELOW_D
+#define CSA_FWD_LDG_BELOW_D 512
+#endif
 inline bool fwd_prefers_ldg(int r, int coff, int d) {
-  return coff * r <= CSA_FWD_LDG_MAX_WINDOW || d < 512;
+  return coff * r <= CSA_FWD_LDG_MAX_WINDOW || d < CSA_FWD_LDG_BELOW_D;
 }
 
 inline bool plan_fwd_ldg(int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
