@@ -545,7 +545,7 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
   if (depth < 3) return false;
   if ((size_t)pl.slots + 2 > depth) pl.slots = (int)depth - 2;  // keep the ring ahead of the consumers
   pl.depth = (int)depth;
-  pl.threads = nc + 32;
+  pl.threads = nc + (bwd ? 64 : 32);  // + producer warp (+ zero warp)
   pl.ape_off = (int)ape_off;
   pl.pre_off = (int)pre_off;
   pl.ring_off = (int)ring_off;
@@ -635,7 +635,7 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit
   const size_t depth = std::min<size_t>(16, (smem_limit - ring_off - 1024) / per_stage);
   if (depth <= (size_t)ng) return false;  // every consumer group needs a stage of its own
   pl.depth = (int)depth;
-  pl.threads = ng * kThreads + (bwd ? 64 : 32);  // + producer warp (+ store warp)
+  pl.threads = ng * kThreads + (bwd ? 96 : 32);  // + producer warp (+ store and zero warps)
   pl.ape_off = (int)ape_off;
   pl.ring_off = (int)ring_off;
   pl.smem = ring_off + 1024 + depth * per_stage;

@@ -11,7 +11,8 @@
 // backward writes each slot's dKV and dScore over the kv and score values it has consumed in
 // the stage (every slot has exactly one reader and writer), and a store warp copies the
 // finished tiles out with tensor-map bulk stores, whole 128-byte tile rows at a time, before
-// it hands the stage back to the producer.
+// it hands the stage back to the producer. A zero warp writes the zeros of short segments
+// and of the rows outside [cu[0], cu[S]) meanwhile.
 //
 // Consumers are NG groups of 8 warps; group h takes the rows h, h+NG, ... of the CTA's
 // range (more groups keep more warps in flight where registers allow). Warp wi of a
@@ -76,7 +77,7 @@ __device__ __forceinline__ void sts_words2(void* p, uint32_t a, uint32_t b) {
 __device__ __forceinline__ int swz(int y, int c) { return y * 128 + ((c ^ (y & 7)) << 4); }
 
 template <int PP, int NG, bool BWD>
-__global__ void __launch_bounds__(NG * kThreads + (BWD ? 64 : 32), 1)
+__global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     pool_long_kernel(const PoolParams p, const __grid_constant__ CUtensorMap tm_kv,
                      const __grid_constant__ CUtensorMap tm_sc,
                      const __grid_constant__ CUtensorMap tm_dkv,
@@ -166,6 +167,26 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 64 : 32), 1)
         }
       }
     }
+    if (BWD && tid >= NCT + 64) {
+      // the zero warp: the zeros of short segments and of this row group's share of the
+      // rows outside [cu[0], cu[S]), over this slice, while the consumers run
+      const int zt = tid - NCT - 64;
+      const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
+      const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
+      for (int s = s_lo; s < s_hi; ++s) {
+        const int a = sCu[s], b = sCu[s + 1];
+        if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, kLongSlice / VEC, zt, 32);
+      }
+      const int64_t c_first = sCu[0];
+      const int64_t c_last = sCu[p.S];
+      const int64_t npad = c_first + (p.capacity - c_last);
+      const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
+      const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
+      const int64_t h0 = min(q1, c_first);
+      if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, kLongSlice / VEC, zt, 32);
+      const int64_t t0 = max(q0, c_first), t1 = q1;
+      if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, kLongSlice / VEC, zt, 32);
+    }
     // ------------------------------ producer ------------------------------------------
     if (tid == NCT) {
       const uint64_t pol = l2_evict_first_policy();
@@ -245,23 +266,6 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 64 : 32), 1)
         sAp[w] = a;
       }
     }
-  }
-  if constexpr (BWD) {  // short segments and rows outside [cu[0], cu[S]) of this slice
-    const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
-    const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
-    for (int s = s_lo; s < s_hi; ++s) {
-      const int a = sCu[s], b = sCu[s + 1];
-      if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, kLongSlice / VEC, tid, NCT);
-    }
-    const int64_t c_first = sCu[0];
-    const int64_t c_last = sCu[p.S];
-    const int64_t npad = c_first + (p.capacity - c_last);
-    const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
-    const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
-    const int64_t h0 = min(q1, c_first);
-    if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, kLongSlice / VEC, tid, NCT);
-    const int64_t t0 = max(q0, c_first), t1 = q1;
-    if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, kLongSlice / VEC, tid, NCT);
   }
   if constexpr (!kApReg) asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // ape staged
 

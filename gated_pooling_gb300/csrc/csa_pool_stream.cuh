@@ -19,7 +19,8 @@
 // chunk in both halves; NC/(d/VEC) rows are computed at once (row j -> row slot j mod
 // slots). Columns are processed in pairs with the f32x2 instructions. ratio and coff are
 // template parameters, so the window layout is static. No thread holds data in flight
-// in registers; every wait is bounded.
+// in registers; every wait is bounded. The backward has one more warp, which writes the
+// zeros of segments shorter than ratio and of the padding rows while the others stream.
 #pragma once
 
 #include <type_traits>
@@ -29,7 +30,8 @@
 namespace csa {
 
 template <int VEC, int NC, int R, int COFF, bool BWD>
-__global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREAM_FWD_CTAS)
+__global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
+                                  BWD ? CSA_STREAM_BWD_CTAS : CSA_STREAM_FWD_CTAS)
     pool_stream_kernel(const PoolParams p) {
   constexpr int NW = VEC / 2;               // 32-bit words (= column pairs) per chunk
   constexpr int AW = VEC >= 4 ? 4 : 2;      // ape values per shared-memory vector
@@ -101,11 +103,11 @@ __global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREA
   if (tid >= NC) {
     // ------------------------------ producer ------------------------------------------
     // the producer warp's lanes issue the previous block's 2*R row copies together; lane 0
-    // then streams the stages
+    // then streams the stages. (lane >= 32: the backward's zero warp)
     const int lane = tid - NC;
     const uint64_t pol = l2_evict_first_policy();
     int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
-    if (need_pre) {
+    if (need_pre && lane < 32) {
       if (lane == 0) mbar_arrive_expect_tx(pre_bar, static_cast<uint32_t>(2 * R * d * 2));
       __syncwarp();
       if (lane < 2 * R) {
@@ -115,6 +117,26 @@ __global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREA
         bulk_load_hint(pre + (sc ? kv_bytes : 0) + w * C * 2, (sc ? p.score : p.kv) + off,
                        d * 2, pre_bar, pol);
       }
+    }
+    if (BWD && lane >= 32) {
+      // the zero warp (backward): the zeros of segments shorter than ratio and of this row
+      // group's share of the padding rows, written while the consumers stream
+      const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
+      const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
+      for (int s2 = s_lo; s2 < s_hi; ++s2) {
+        const int a = sCu[s2];
+        const int b = sCu[s2 + 1];
+        if (b - a < R && b > a) zero_rows<NW>(p, a, b - a, V, lane - 32, 32);
+      }
+      const int64_t c_first = sCu[0];
+      const int64_t c_last = sCu[p.S];
+      const int64_t npad = c_first + (p.capacity - c_last);
+      const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
+      const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
+      const int64_t h0 = min(q1, c_first);
+      if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, V, lane - 32, 32);
+      const int64_t t0 = max(q0, c_first), t1 = q1;
+      if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, V, lane - 32, 32);
     }
     if (lane == 0) {
       int j = 0;
@@ -148,9 +170,7 @@ __global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREA
   } else {
     // ------------------------------ consumers -----------------------------------------
     // While the first stages are in flight: stage ape (scaled by log2 e) as
-    // [w][h][chunk] vectors of AW values (a chunk's vectors are V apart) and, backward,
-    // write the zeros of segments shorter than ratio and of the padding rows of this row
-    // group.
+    // [w][h][chunk] vectors of AW values (a chunk's vectors are V apart).
     {
       ApeVec* dstA = reinterpret_cast<ApeVec*>(smem + p.ape_off);
       auto put = [&](const int it, ApeVec a) {
@@ -163,24 +183,6 @@ __global__ void __launch_bounds__(NC + 32, BWD ? CSA_STREAM_BWD_CTAS : CSA_STREA
         dstA[it] = a;
       };
       for (int it = tid; it < W * NA * V; it += NC) put(it, __ldg(ape_src(it)));
-    }
-    if constexpr (BWD) {
-      const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
-      const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
-      for (int s = s_lo; s < s_hi; ++s) {
-        const int a = sCu[s];
-        const int b = sCu[s + 1];
-        if (b - a < R && b > a) zero_rows<NW>(p, a, b - a, V, tid, NC);
-      }
-      const int64_t c_first = sCu[0];
-      const int64_t c_last = sCu[p.S];
-      const int64_t npad = c_first + (p.capacity - c_last);
-      const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
-      const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
-      const int64_t h0 = min(q1, c_first);
-      if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, V, tid, NC);
-      const int64_t t0 = max(q0, c_first), t1 = q1;
-      if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, V, tid, NC);
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");  // consumers only
 
