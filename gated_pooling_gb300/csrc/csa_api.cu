@@ -239,10 +239,10 @@ __device__ __forceinline__ void neumaier_add(float& s, float& c, float x) {
 // dAPE = (accumulate ? dAPE : 0) + sum over row groups g = 0..R-1 of partial[g]. A block
 // covers 32 entries with SPLIT warps; warp k adds the contiguous row-group range
 // [k*R/SPLIT, (k+1)*R/SPLIT) (loaded kReduceBatch at a time, so the loads overlap) with
-// compensated fp32 sums, then warp 0 adds the range sums in order. SPLIT follows R (about
-// five partials per warp), so that few threads idle. The result is the same bits on every
-// run. Launched as a programmatic dependent of the pooling kernel: it may start early and
-// waits for that grid's results.
+// compensated fp32 sums; the range sums are then combined pairwise in a fixed tree. SPLIT
+// follows R (about five partials per warp), so that few threads idle. The result is the
+// same bits on every run. Launched as a programmatic dependent of the pooling kernel: it
+// may start early and waits for that grid's results.
 constexpr int kReduceCols = 32;
 constexpr int kReduceBatch = 12;  // partials a thread has in flight at once
 template <int SPLIT>
@@ -273,14 +273,24 @@ __global__ void __launch_bounds__(kReduceCols * SPLIT)
   }
   s_sum[k][lane] = s;
   s_cmp[k][lane] = c;
+  // the range sums, combined pairwise in a fixed tree (ranges k and k + h, h = SPLIT/2,
+  // SPLIT/4, ..., 1), carrying each side's compensation
+  for (int h = kReduceSplit / 2; h >= 1; h /= 2) {
+    __syncthreads();
+    if (k < h) {
+      float t = s_sum[k][lane], tc = s_cmp[k][lane];
+      neumaier_add(t, tc, s_sum[k + h][lane]);
+      neumaier_add(t, tc, s_cmp[k + h][lane]);
+      s_sum[k][lane] = t;
+      s_cmp[k][lane] = tc;
+    }
+  }
   __syncthreads();
   if (k == 0 && e < n) {
     float t = 0.f, tc = 0.f;
     if (accumulate) neumaier_add(t, tc, dape[e]);
-    for (int kk = 0; kk < kReduceSplit; ++kk) {
-      neumaier_add(t, tc, s_sum[kk][lane]);
-      neumaier_add(t, tc, s_cmp[kk][lane]);
-    }
+    neumaier_add(t, tc, s_sum[0][lane]);
+    neumaier_add(t, tc, s_cmp[0][lane]);
     dape[e] = t + tc;
   }
 }

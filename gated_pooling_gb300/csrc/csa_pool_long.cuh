@@ -102,12 +102,26 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   uint64_t* empty = full + p.depth;
   uint64_t* done = empty + p.depth;  // backward: a group has written the stage's gradients
 
+  const int tid = threadIdx.x;
+  // mbarriers, one per thread, before the map is read (their set-up does not depend on
+  // it): the CTA-scope proxy fence makes them visible to the bulk-copy engine, the
+  // barriers inside the block prefix to the other threads
+  {
+    const int nb = (BWD ? 3 : 2) * p.depth;
+    if (tid < nb) {
+      const int k = tid / p.depth, i = tid % p.depth;
+      if (k == 0) mbar_init(&full[i], 1);
+      else if (k == 1) mbar_init(&empty[i], BWD ? 1 : kThreads);  // backward: store warp
+      else mbar_init(&done[i], kThreads);
+      fence_proxy_async_smem();
+    }
+    if (tid == 0) s_abort = 0;
+  }
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
   if (TC < 0) return;
   if constexpr (BWD) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  const int tid = threadIdx.x;
   const int r = p.r, d = p.d, C = p.C;
   const bool two = p.coff == 2;
   const int col0 = blockIdx.x * kLongSlice;  // first column of the slice (in a half)
@@ -116,16 +130,6 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
   const int nrows = o1 - o0;
 
-  if (tid == 0) {
-    s_abort = 0;
-    for (int i = 0; i < p.depth; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], BWD ? 1 : kThreads);  // backward: released by the store warp
-      if constexpr (BWD) mbar_init(&done[i], kThreads);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
 
   if (tid >= NCT) {
     if constexpr (BWD) {
