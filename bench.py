@@ -33,11 +33,13 @@ METRIC = "fwd+bwd µs and achieved HBM GB/s (% of GB300 roofline) per THD pack"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-# DRAM bytes (read + write) per backward call on the headline pack, from one ncu capture
-# of this build: pool kernel 108.28 MB read + 47.77 MB write (the rest of its writes are
-# still dirty in L2 when it ends), reduction 2.50 MB read (the capture's summary is kept
-# with the profiles). It must be re-measured whenever a kernel changes.
-ROOFLINE_TRAFFIC = {"3x8192_d512": 108.281088e6 + 47.766016e6 + 2.49856e6}
+# DRAM bytes (read + write) per backward call, from one ncu capture of this build (the
+# summaries are kept with the profiles): headline pack, pool kernel 108.28 MB read +
+# 47.03 MB write (the rest of its writes are still dirty in L2 when it ends), reduction
+# 2.50 MB read; long-window pack, pool kernel 135.66 + 82.83 MB, reduction 4.99 MB. It
+# must be re-measured whenever a kernel changes.
+ROOFLINE_TRAFFIC = {"3x8192_d512": 108.280576e6 + 47.028992e6 + 2.500352e6,
+                    "long_r128_d512": 135.660544e6 + 82.827264e6 + 4.98944e6}
 
 
 # ----------------------------------------------------------------------------------
