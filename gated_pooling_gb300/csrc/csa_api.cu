@@ -1,5 +1,6 @@
 // csa_api.cu -- the C ABI of the GB300 CSA/HCA compressor pooling: argument checks,
 // launch planning, the index-map test hook and the fixed-order dAPE reduction.
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -82,6 +83,7 @@ cudaError_t blocks_per_sm(int dev, const void* kernel, int threads, size_t smem,
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // 2-D tensor maps for the long-window kernel, encoded through the driver entry point the
 // runtime hands out (no link against the driver library).
@@ -124,7 +126,6 @@ csa_status_t check_sizes(int32_t S, int32_t ratio, int32_t coff, int32_t d, int6
                          int64_t out_rows) {
   if (S < 0 || ratio < 1 || d < 1 || capacity < 0 || out_rows < 0) return CSA_ERR_INVALID_VALUE;
   if (coff != 1 && coff != 2) return CSA_ERR_UNSUPPORTED;
-  if (d % 8 != 0) return CSA_ERR_UNSUPPORTED;
   if (S > CSA_MAX_SEGMENTS) return CSA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(coff) * ratio > CSA_MAX_WINDOW) return CSA_ERR_UNSUPPORTED;
   const int64_t C = static_cast<int64_t>(coff) * d;
@@ -135,9 +136,12 @@ csa_status_t check_sizes(int32_t S, int32_t ratio, int32_t coff, int32_t d, int6
   return CSA_OK;
 }
 
-// Plan plus the device-dependent row-group count R.
+static_assert(kGenericMaxWindow == CSA_MAX_GENERIC_WINDOW, "generic window limit");
+
+// Plan plus the device-dependent row-group count R. `fast`: d % 8 == 0 and every pointer
+// 16-byte aligned (the vector kernels); otherwise the generic scalar kernel.
 csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t d,
-                       int64_t out_rows, Plan* pl, PoolKernel* kernel) {
+                       int64_t out_rows, bool fast, Plan* pl, PoolKernel* kernel) {
   int dev = 0, sms = 0, bps = 0, optin = 0;
   if (note(cudaGetDevice(&dev)) != cudaSuccess) return CSA_ERR_CUDA;
   if (device_sms(dev, &sms) != cudaSuccess) return CSA_ERR_CUDA;
@@ -146,19 +150,26 @@ csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t
     return CSA_ERR_CUDA;
   // Forward windows of <= 8 positions (or narrow rows) take the register-load kernel, other
   // windows of <= 8 positions the block-streaming kernel, windows of 16..128 positions with
-  // d % 64 == 0 the tensor-copy kernel, everything else the split kernel.
+  // d % 64 == 0 the tensor-copy kernel, everything else the split kernel; shapes or
+  // pointers the vector kernels cannot take go to the generic kernel.
   const size_t limit = static_cast<size_t>(optin) - 256;  // static shared memory headroom
-  if (!(!bwd && plan_fwd_ldg(S, ratio, coff, d, limit, pl)) &&
-      !plan_stream(bwd, S, ratio, coff, d, limit, pl) &&
-      !(encode_fn() != nullptr && plan_long(bwd, S, ratio, coff, d, limit, pl)))
+  if (!fast) {
+    if (!plan_generic(bwd, S, ratio, coff, d, limit, pl)) return CSA_ERR_UNSUPPORTED;
+  } else if (!(!bwd && plan_fwd_ldg(S, ratio, coff, d, limit, pl)) &&
+             !plan_stream(bwd, S, ratio, coff, d, limit, pl) &&
+             !(encode_fn() != nullptr && plan_long(bwd, S, ratio, coff, d, limit, pl))) {
     *pl = plan_shape(bwd, S, ratio, coff, d);
+  }
   *kernel = bwd ? bwd_kernel_for(*pl) : fwd_kernel_for(*pl);
   if (*kernel == nullptr) return CSA_ERR_UNSUPPORTED;
   if (blocks_per_sm(dev, reinterpret_cast<const void*>(*kernel), pl->threads, pl->smem, &bps) !=
       cudaSuccess)
     return CSA_ERR_CUDA;
   if (bps < 1) return CSA_ERR_UNSUPPORTED;  // shared memory of the plan does not fit
-  const int64_t want = (static_cast<int64_t>(sms) * bps + pl->K - 1) / pl->K;
+  int64_t want = (static_cast<int64_t>(sms) * bps + pl->K - 1) / pl->K;
+  // the generic kernel's many small CTAs: at most one row group per SM, so that its dAPE
+  // partials need no more workspace than the vector kernels'
+  if (pl->generic && want > sms) want = sms;
   const int64_t cap = out_rows > 0 ? out_rows : 1;
   int64_t R = want < cap ? want : cap;
   if (R < 1) R = 1;
@@ -330,7 +341,7 @@ const char* csa_status_string(int status) {
   switch (status) {
     case CSA_OK: return "CSA_OK";
     case CSA_ERR_INVALID_VALUE: return "CSA_ERR_INVALID_VALUE: null, negative, misaligned or too small argument";
-    case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: coff not in {1,2}, d % 8 != 0, or a size limit exceeded";
+    case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: coff not in {1,2}, or a size limit exceeded";
     case CSA_ERR_CUDA: return "CSA_ERR_CUDA: a CUDA runtime call or kernel launch failed";
     default: return "unknown csa status";
   }
@@ -359,11 +370,14 @@ csa_status_t csa_compressor_fwd(const void* kv, const void* score, const float* 
   if (cu_seqlens == nullptr || ape == nullptr) return CSA_ERR_INVALID_VALUE;
   if (capacity > 0 && (kv == nullptr || score == nullptr)) return CSA_ERR_INVALID_VALUE;
   if (out_rows > 0 && out == nullptr) return CSA_ERR_INVALID_VALUE;
-  if (!aligned16(kv) || !aligned16(score) || !aligned16(ape) || !aligned16(out))
+  if (!aligned_to(kv, 2) || !aligned_to(score, 2) || !aligned_to(ape, 4) || !aligned_to(out, 2))
     return CSA_ERR_INVALID_VALUE;
+  const bool fast = d % 8 == 0 && aligned16(kv) && aligned16(score) && aligned16(ape) &&
+                    aligned16(out);
+  if (!fast && coff * ratio > CSA_MAX_GENERIC_WINDOW) return CSA_ERR_UNSUPPORTED;
   Plan pl;
   PoolKernel k;
-  st = make_plan(false, S, ratio, coff, d, out_rows, &pl, &k);
+  st = make_plan(false, S, ratio, coff, d, out_rows, fast, &pl, &k);
   if (st != CSA_OK) return st;
   PoolParams p = base_params(pl, kv, score, ape, cu_seqlens, S, ratio, coff, d, capacity,
                              out_rows, dev_error);
@@ -374,10 +388,17 @@ csa_status_t csa_compressor_fwd(const void* kv, const void* score, const float* 
 size_t csa_compressor_bwd_workspace_bytes(int32_t S, int32_t ratio, int32_t coff, int32_t d,
                                           int64_t capacity, int64_t out_rows) {
   if (check_sizes(S, ratio, coff, d, capacity, out_rows) != CSA_OK) return 0;
-  Plan pl;
-  PoolKernel k;
-  if (make_plan(true, S, ratio, coff, d, out_rows, &pl, &k) != CSA_OK) return 0;
-  return static_cast<size_t>(pl.R) * ratio * coff * d * sizeof(float);
+  // enough for whichever kernel the call's pointers select
+  size_t need = 0;
+  for (int fast = 0; fast < 2; ++fast) {
+    if (fast && d % 8 != 0) continue;
+    if (!fast && coff * ratio > CSA_MAX_GENERIC_WINDOW) continue;
+    Plan pl;
+    PoolKernel k;
+    if (make_plan(true, S, ratio, coff, d, out_rows, fast != 0, &pl, &k) != CSA_OK) continue;
+    need = std::max(need, static_cast<size_t>(pl.R) * ratio * coff * d * sizeof(float));
+  }
+  return need;
 }
 
 csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* ape,
@@ -392,12 +413,17 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
   if (capacity > 0 && (kv == nullptr || score == nullptr || dkv == nullptr || dscore == nullptr))
     return CSA_ERR_INVALID_VALUE;
   if (out_rows > 0 && dout == nullptr) return CSA_ERR_INVALID_VALUE;
-  if (!aligned16(kv) || !aligned16(score) || !aligned16(ape) || !aligned16(dout) ||
-      !aligned16(dkv) || !aligned16(dscore) || !aligned16(dape) || !aligned16(workspace))
+  if (!aligned_to(kv, 2) || !aligned_to(score, 2) || !aligned_to(ape, 4) ||
+      !aligned_to(dout, 2) || !aligned_to(dkv, 2) || !aligned_to(dscore, 2) ||
+      !aligned_to(dape, 4) || !aligned_to(workspace, 4))
     return CSA_ERR_INVALID_VALUE;
+  const bool fast = d % 8 == 0 && aligned16(kv) && aligned16(score) && aligned16(ape) &&
+                    aligned16(dout) && aligned16(dkv) && aligned16(dscore) && aligned16(dape) &&
+                    aligned16(workspace);
+  if (!fast && coff * ratio > CSA_MAX_GENERIC_WINDOW) return CSA_ERR_UNSUPPORTED;
   Plan pl;
   PoolKernel k;
-  st = make_plan(true, S, ratio, coff, d, out_rows, &pl, &k);
+  st = make_plan(true, S, ratio, coff, d, out_rows, fast, &pl, &k);
   if (st != CSA_OK) return st;
   const size_t need = static_cast<size_t>(pl.R) * ratio * coff * d * sizeof(float);
   if (workspace == nullptr || workspace_bytes < need) return CSA_ERR_INVALID_VALUE;

@@ -1,12 +1,14 @@
 // csa_bwd.cu -- backward instantiations of the pooling kernel (4 columns per thread,
 // so that the per-thread dAPE sums fit in registers).
 #include "csa_internal.h"
+#include "csa_pool_generic.cuh"
 #include "csa_pool_long.cuh"
 #include "csa_pool_stream.cuh"
 
 namespace csa {
 
 PoolKernel bwd_kernel_for(const Plan& pl) {
+  if (pl.generic) return pool_generic_kernel<true>;
   if (pl.longk) {
     switch (pl.pp) {
       case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_BWD_GROUPS, true>);

@@ -1,5 +1,6 @@
 // csa_fwd.cu -- forward instantiations of the pooling kernel (8 columns per thread).
 #include "csa_internal.h"
+#include "csa_pool_generic.cuh"
 #include "csa_pool_long.cuh"
 #include "csa_fwd_ldg.cuh"
 #include "csa_pool_stream.cuh"
@@ -7,6 +8,7 @@
 namespace csa {
 
 PoolKernel fwd_kernel_for(const Plan& pl) {
+  if (pl.generic) return pool_generic_kernel<false>;
   if (pl.longk) {
     switch (pl.pp) {
       case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, false>);

@@ -434,6 +434,7 @@ struct Plan {
   bool tma = false;  // block-streaming kernel (bulk copies) for windows of <= 8 positions
   bool ldg = false;  // forward through register loads (csa_fwd_ldg.cuh)
   bool longk = false;  // long windows through 2-D tensor copies (csa_pool_long.cuh)
+  bool generic = false;  // any head dim / alignment, scalar (csa_pool_generic.cuh)
   int box_rows = 0;    // long windows: tokens per tensor box
   int coff = 0;
   int threads = kThreads;
@@ -639,6 +640,33 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit
   pl.ape_off = (int)ape_off;
   pl.ring_off = (int)ring_off;
   pl.smem = ring_off + 1024 + depth * per_stage;
+  *out = pl;
+  return true;
+}
+
+// Generic geometry (csa_pool_generic.cuh): 128 threads = 128 columns of each half per CTA,
+// grid = ceil(d/128) column slices x R row groups; the backward keeps W x 128 fp32 dAPE
+// sums in shared memory. Returns false for windows above the generic limit.
+constexpr int kGenericMaxWindow = 256;
+inline bool plan_generic(bool bwd, int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
+  const int W = coff * r;
+  if (W > kGenericMaxWindow) return false;
+  Plan pl;
+  pl.generic = true;
+  pl.coff = coff;
+  pl.vec = 1;
+  pl.pp = W;
+  pl.P = 1;
+  pl.V = d;
+  pl.Vs = 128;
+  pl.K = (d + 127) / 128;
+  pl.slots = 1;
+  pl.sB_words = ((S + 1) + 3) & ~3;
+  const size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
+  pl.ape_off = (int)ape_off;
+  pl.smem = ape_off + (bwd ? (size_t)W * 128 * 4 : 0);
+  if (pl.smem > smem_limit) return false;
+  pl.threads = 128;
   *out = pl;
   return true;
 }

@@ -27,8 +27,11 @@
  *     synchronises, and never reads device memory from the host.
  *   - Work is enqueued on `stream` (NULL: the legacy default stream) of the current
  *     device; calls return as soon as it is enqueued.
- *   - bf16 tensors are row-major, contiguous, 16-byte aligned; ape is fp32, 16-byte
- *     aligned. d must be a multiple of 8.
+ *   - bf16 tensors are row-major and contiguous, fp32 tensors (ape, dape, workspace) too.
+ *     Pointers need their natural alignment (2 bytes for bf16, 4 for fp32). The fast
+ *     kernels run when d is a multiple of 8 and every pointer is 16-byte aligned; any
+ *     other shape takes a scalar kernel, which accepts windows (coff * ratio) of up to
+ *     CSA_MAX_GENERIC_WINDOW positions.
  *   - Host-side argument checks return a status and enqueue nothing. Problems that
  *     only the device can see (cu_seqlens decreasing, negative or past capacity;
  *     more blocks than out_rows) make the kernels write a code to *dev_error (when
@@ -52,7 +55,7 @@ typedef struct CUstream_st* csa_stream_t;
 typedef enum {
   CSA_OK = 0,
   CSA_ERR_INVALID_VALUE = 1, /* NULL pointer, negative size, misaligned pointer, small workspace */
-  CSA_ERR_UNSUPPORTED = 2,   /* coff not in {1,2}, d % 8 != 0, size limits below */
+  CSA_ERR_UNSUPPORTED = 2,   /* coff not in {1,2}, size limits below */
   CSA_ERR_CUDA = 3           /* a CUDA runtime call or kernel launch failed */
 } csa_status_t;
 
@@ -65,6 +68,7 @@ typedef enum {
 /* Limits checked on the host (CSA_ERR_UNSUPPORTED beyond them). */
 #define CSA_MAX_SEGMENTS 16384   /* S */
 #define CSA_MAX_WINDOW 2048      /* coff * ratio */
+#define CSA_MAX_GENERIC_WINDOW 256 /* coff * ratio when d % 8 != 0 or a pointer is not 16-byte aligned */
 #define CSA_MAX_ELEMS 2147483647 /* capacity*coff*d and out_rows*d must stay below 2^31 */
 
 /* Text for a status code (static storage). */

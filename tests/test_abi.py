@@ -76,7 +76,7 @@ def bwd_status(lib, **over):
 @pytest.mark.parametrize("over,code", [
     (dict(coff=0), gp.CSA_ERR_UNSUPPORTED),
     (dict(coff=3), gp.CSA_ERR_UNSUPPORTED),
-    (dict(d=12), gp.CSA_ERR_UNSUPPORTED),
+    (dict(d=12, ratio=200), gp.CSA_ERR_UNSUPPORTED),  # d % 8 != 0: generic, window 400 > 256
     (dict(S=20000), gp.CSA_ERR_UNSUPPORTED),
     (dict(ratio=2048), gp.CSA_ERR_UNSUPPORTED),          # window 4096 > 2048
     (dict(capacity=1 << 28, d=64), gp.CSA_ERR_UNSUPPORTED),  # capacity*coff*d >= 2^31
@@ -90,8 +90,10 @@ def bwd_status(lib, **over):
     (dict(ape=None), gp.CSA_ERR_INVALID_VALUE),
     (dict(kv=None), gp.CSA_ERR_INVALID_VALUE),
     (dict(out=None), gp.CSA_ERR_INVALID_VALUE),
-    (dict(kv=FAKE + 8), gp.CSA_ERR_INVALID_VALUE),      # misaligned
-    (dict(out=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),
+    (dict(kv=FAKE + 1), gp.CSA_ERR_INVALID_VALUE),      # misaligned for bf16
+    (dict(ape=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),     # misaligned for fp32
+    (dict(out=FAKE + 1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(out=FAKE + 2, ratio=200), gp.CSA_ERR_UNSUPPORTED),  # unaligned: generic, window too long
 ])
 def test_fwd_rejects(lib, over, code):
     assert fwd_status(lib, **over) == code
@@ -99,13 +101,14 @@ def test_fwd_rejects(lib, over, code):
 
 @pytest.mark.parametrize("over,code", [
     (dict(coff=3), gp.CSA_ERR_UNSUPPORTED),
-    (dict(d=4), gp.CSA_ERR_UNSUPPORTED),
+    (dict(d=4, ratio=129), gp.CSA_ERR_UNSUPPORTED),  # generic, window 258 > 256
     (dict(dape=None), gp.CSA_ERR_INVALID_VALUE),
     (dict(dkv=None), gp.CSA_ERR_INVALID_VALUE),
     (dict(dscore=None), gp.CSA_ERR_INVALID_VALUE),
     (dict(dout=None), gp.CSA_ERR_INVALID_VALUE),
-    (dict(dscore=FAKE + 4), gp.CSA_ERR_INVALID_VALUE),
-    (dict(ws=FAKE + 4), gp.CSA_ERR_INVALID_VALUE),
+    (dict(dscore=FAKE + 1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(dape=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),
+    (dict(ws=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),
     (dict(ratio=-2), gp.CSA_ERR_INVALID_VALUE),
 ])
 def test_bwd_rejects(lib, over, code):
@@ -114,7 +117,7 @@ def test_bwd_rejects(lib, over, code):
 
 def test_workspace_query_rejects_bad_sizes(lib):
     assert gp.csa_compressor_bwd_workspace_bytes(1, 4, 3, 8, 8, 2) == 0
-    assert gp.csa_compressor_bwd_workspace_bytes(1, 4, 2, 12, 8, 2) == 0
+    assert gp.csa_compressor_bwd_workspace_bytes(1, 200, 2, 12, 8, 2) == 0  # generic, window > 256
 
 
 def test_map_blocks_rejects(lib):

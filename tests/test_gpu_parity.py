@@ -5,7 +5,8 @@ times) and small packs that exercise every window shape the kernels specialise o
 ragged packs, segments shorter than ratio, empty segments, tails, padding rows before
 cu_seqlens[0] and after cu_seqlens[S], coff 1 and 2, ratios 1..128, split windows, the
 tensor-copy kernel's window sizes 16..128, head dims whose chunk count does not fill a
-column slice, S = 0 and capacity 0.
+column slice, head dims that are not a multiple of 8 and pointers off 16-byte boundaries
+(the generic kernel), S = 0 and capacity 0.
 The tolerance is the one tests/parity.py derives; the count of elements that needed
 its cancellation clause is capped.
 """
@@ -51,6 +52,17 @@ def small_packs():
         "r64c2_d64": ts.make_custom([260, 70, 10], ratio=64, coff=2, d=64, pad_rows=3, seed=25,
                                     score_scale=4.0),
         "r16c1_d64": ts.make_custom([50, 16, 5], ratio=16, coff=1, d=64, pad_rows=0, seed=26),
+        # generic kernel: head dims that are not a multiple of 8 (several column slices,
+        # windows up to its 256-position limit)
+        "g_d65_r4c2": ts.make_custom([37, 12, 3, 20], ratio=4, coff=2, d=65, pad_rows=3, seed=30),
+        "g_d13_r3c1": ts.make_custom([10, 2, 17], ratio=3, coff=1, d=13, pad_rows=2, seed=31),
+        "g_d130_r2c2": ts.make_custom([9, 1, 14, 33], ratio=2, coff=2, d=130, pad_rows=4,
+                                      seed=32),
+        "g_d65_r128c1": ts.make_custom([300, 129, 50], ratio=128, coff=1, d=65, pad_rows=3,
+                                       seed=33, score_scale=4.0),
+        "g_d9_r16c2": ts.make_custom([70, 33, 15], ratio=16, coff=2, d=9, pad_rows=2, seed=34),
+        "g_d201_r128c2": ts.make_custom([400, 256, 100], ratio=128, coff=2, d=201, pad_rows=1,
+                                        seed=35),
         "r128c2_split_d32": ts.make_custom([400, 128, 127], ratio=128, coff=2, d=32, pad_rows=3,
                                            seed=12),
         "all_short": ts.make_custom([1, 2, 3], ratio=4, coff=2, d=8, pad_rows=2, seed=13),
@@ -72,9 +84,9 @@ SMALL = small_packs()
 FULL = ["tiny", "1x8192_d128", "3x8192_d512", "ragged_r2_d512", "long_r128_d512"]
 
 
-def check_fwd(gp, pack):
+def check_fwd(gp, pack, shift=0):
     ref = oracle.fwd_pack(pack, want_f64=True, want_err=True)
-    got, err = H.run_fwd(gp, pack)
+    got, err = H.run_fwd(gp, pack, shift=shift)
     assert err == 0
     rep = compare_bf16("out", got, ref["out"], ref["out_f64"], ref["out_err"])
     print(pack.name, rep)
@@ -83,9 +95,9 @@ def check_fwd(gp, pack):
     return rep
 
 
-def check_bwd(gp, pack):
+def check_bwd(gp, pack, shift=0):
     ref = oracle.bwd_pack(pack, want_f64=True, want_err=True, want_owners=True)
-    dkv, dsc, dape, err = H.run_bwd(gp, pack)
+    dkv, dsc, dape, err = H.run_bwd(gp, pack, shift=shift)
     assert err == 0
     r1 = compare_bf16("dkv", dkv, ref["dkv"], ref["dkv_f64"], np.abs(ref["dkv_f64"]))
     r2 = compare_bf16("dscore", dsc, ref["dscore"], ref["dscore_f64"], ref["dscore_err"])
@@ -110,6 +122,21 @@ def test_fwd_small(cuda_lib, name):
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_bwd_small(cuda_lib, name):
     check_bwd(cuda_lib, SMALL[name])
+
+
+# pointers 2 (bf16) / 4 (fp32) bytes past a 16-byte boundary: the generic kernel, on shapes
+# the vector kernels would otherwise take
+MISALIGNED = ["tiny", "r4c2_d264", "r2c2_short_d64", "r16c1_d64", "r8c2_d128"]
+
+
+@pytest.mark.parametrize("name", MISALIGNED)
+def test_fwd_misaligned(cuda_lib, name):
+    check_fwd(cuda_lib, SMALL[name], shift=1)
+
+
+@pytest.mark.parametrize("name", MISALIGNED)
+def test_bwd_misaligned(cuda_lib, name):
+    check_bwd(cuda_lib, SMALL[name], shift=1)
 
 
 @pytest.mark.parametrize("name", FULL)
