@@ -1,5 +1,6 @@
-// csa_bwd.cu -- backward instantiations of the pooling kernel (4 columns per thread,
-// so that the per-thread dAPE sums fit in registers).
+// csa_bwd.cu -- backward instantiations of the pooling kernels (generic, long window,
+// block streaming with 4 columns per thread so that the per-thread dAPE sums fit in
+// registers, split window) and the plan -> kernel choice.
 #include "csa_internal.h"
 #include "csa_pool_generic.cuh"
 #include "csa_pool_long.cuh"

@@ -1,4 +1,5 @@
-// csa_fwd.cu -- forward instantiations of the pooling kernel (8 columns per thread).
+// csa_fwd.cu -- forward instantiations of the pooling kernels (generic, long window,
+// register loads, block streaming, split window) and the plan -> kernel choice.
 #include "csa_internal.h"
 #include "csa_pool_generic.cuh"
 #include "csa_pool_long.cuh"

@@ -469,16 +469,17 @@ inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
 // Block-streaming kernel shape: columns per thread and consumer threads, per direction.
 // The backward keeps 4 columns per thread so that its per-thread dAPE sums and softmax
 // weights stay in registers.
-// CTAs per SM, per direction. Two forward CTAs per SM (two producers, each with half the
-// ring) read faster through bulk copies than one; the backward needs its registers.
+// CTAs per SM, per direction: one by default (two forward CTAs, each with half the ring,
+// measured no faster; two backward CTAs run short of registers).
 #ifndef CSA_STREAM_FWD_CTAS
 #define CSA_STREAM_FWD_CTAS 1
 #endif
 #ifndef CSA_STREAM_BWD_CTAS
 #define CSA_STREAM_BWD_CTAS 1
 #endif
-// Consumers plus one producer warp per CTA: 8 consumer warps + 1 producer put at most
-// three warps on an SM sub-partition, a 168-register budget per thread (no spills).
+// Consumers plus one producer warp per CTA (and the backward's zero warp): 8 consumer
+// warps + 1 or 2 more put at most three warps on an SM sub-partition, a 168-register
+// budget per thread (no spills).
 #ifndef CSA_FWD_VEC
 #define CSA_FWD_VEC 8
 #endif
