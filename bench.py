@@ -267,6 +267,10 @@ def run_ours(args, rank, world, local_rank):
         "fwd_us": round(fwd_us, 2), "bwd_us": round(bwd_us, 2),
         "graph_fwd_bwd_us": graph_us,
         "fwd_bytes": fwd_b, "bwd_bytes": bwd_b,
+        "fwd_us_median": round(1e3 * float(np.median(fwd_ms)), 2),
+        "fwd_us_min": round(1e3 * min(fwd_ms), 2),
+        "bwd_us_median": round(1e3 * float(np.median(bwd_ms)), 2),
+        "bwd_us_min": round(1e3 * min(bwd_ms), 2),
         "fwd_gbs": round(fwd_b / (fwd_us * 1e-6) / 1e9, 1), "bwd_gbs": round(bwd_gbs, 1),
         "frac_of_measured_hbm": round(value / world / peak, 4),
         "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),

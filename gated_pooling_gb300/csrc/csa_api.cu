@@ -211,6 +211,26 @@ PoolParams base_params(const Plan& pl, const void* kv, const void* score, const 
   return p;
 }
 
+// Every pooling kernel is launched as a programmatic dependent of the stream's previous
+// kernel (it waits for that grid inside build_block_prefix before touching memory).
+#ifndef CSA_PDL_POOL
+#define CSA_PDL_POOL 1
+#endif
+cudaError_t launch_pdl(const void* k, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       void** args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = CSA_PDL_POOL;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return note(cudaLaunchKernelExC(&cfg, k, args));
+}
+
 csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t stream) {
   if (pl.longk) {
     // tensor maps over kv and score [capacity, C]; with no rows any aligned address will
@@ -229,13 +249,13 @@ csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t st
         !encode_bf16_map(&mdsc, dsc, p.capacity, p.C, sw, pl.box_rows))
       return CSA_ERR_CUDA;
     void* args[] = {&p, &mkv, &msc, &mdkv, &mdsc};
-    cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
-                                          dim3(pl.threads), args, pl.smem, stream));
+    const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
+                                     dim3(pl.threads), pl.smem, stream, args);
     return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
   }
   void* args[] = {&p};
-  cudaError_t e = note(cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
-                                        dim3(pl.threads), args, pl.smem, stream));
+  const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(k), dim3(pl.K, pl.R),
+                                   dim3(pl.threads), pl.smem, stream, args);
   return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
 

@@ -133,6 +133,18 @@ __device__ __forceinline__ int block_exclusive_scan(int val, int* warp_sums, int
   return excl;
 }
 
+// Programmatic dependent launch. The pooling kernels are launched as programmatic
+// dependents of the previous kernel of their stream, so they may start before it has
+// finished; pdl_wait (the first thing build_block_prefix does, before any global memory
+// access) holds them until that grid has completed and its memory is visible. It returns
+// at once when the kernel was launched normally or the previous grid never triggered.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel of the stream, if launched as a programmatic dependent, begin its
+// launch (it still waits for this grid's completion before touching memory).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Builds the block prefix sB[s] = sum_{s' < s} floor(L_s' / ratio), s = 0..S, in shared
 // memory and returns total_comp = sB[S]. Checks cu_seqlens (cu[0] >= 0, non-decreasing,
 // cu[S] <= capacity) and total_comp <= out_rows; on failure thread 0 writes the code to
@@ -141,6 +153,7 @@ __device__ __forceinline__ int build_block_prefix(const int32_t* __restrict__ cu
                                                   int ratio, int64_t capacity, int64_t out_rows,
                                                   int32_t* dev_error, int* sB, int* warp_sums,
                                                   int* sCu = nullptr) {
+  pdl_wait();  // the previous kernel's results (cu_seqlens, inputs) are visible after this
   int carry = 0;
   int bad = 0;
   if (threadIdx.x == 0) {

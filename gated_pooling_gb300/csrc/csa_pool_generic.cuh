@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kGenericThreads) pool_generic_kernel(const Poo
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
   if (TC < 0) return;
-  if constexpr (BWD) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();  // the next kernel (the dAPE reduction, or the caller's) may launch
 
   const int tid = threadIdx.x;
   const int r = p.r, d = p.d, C = p.C, W = p.W;

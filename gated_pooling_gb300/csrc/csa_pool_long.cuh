@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
   if (TC < 0) return;
-  if constexpr (BWD) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();  // the next kernel (the dAPE reduction, or the caller's) may launch
 
   const int r = p.r, d = p.d, C = p.C;
   const bool two = p.coff == 2;

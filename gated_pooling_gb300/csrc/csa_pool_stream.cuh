@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
   const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
   if (TC < 0) return;
-  if constexpr (BWD) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();  // the next kernel (the dAPE reduction, or the caller's) may launch
 
   const int g = blockIdx.y;
   const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
