@@ -9,7 +9,9 @@
 * device-detected errors: bad cu_seqlens and too few out_rows set the error word and
   leave the outputs unwritten;
 * accumulate_dape adds to the current dAPE; a non-default stream works; out_rows larger
-  than total_comp leaves the extra rows untouched.
+  than total_comp leaves the extra rows untouched;
+* a call reads what the previous call on its stream wrote (programmatic launch);
+* fwd + bwd captured in a CUDA graph replay bit for bit on new inputs.
 """
 import numpy as np
 import pytest
@@ -182,3 +184,30 @@ def test_cuda_graph_capture_and_replay(cuda_lib):
         rk, rs, rd, _ = H.run_bwd(cuda_lib, pack)
         assert (got[0] == ref_out).all() and (got[1] == rk).all() and (got[2] == rs).all()
         assert (got[3].view(np.uint32) == rd.view(np.uint32)).all()
+
+
+def test_back_to_back_calls_see_previous_results(cuda_lib):
+    """Every call is launched as a programmatic dependent of the stream's previous kernel,
+    so it may start before that kernel ends; it must still read that kernel's results. A
+    forward call writes its output into a NaN-filled buffer which the next forward call
+    (ratio 1, coff 1: its output is its kv) reads as kv and score, back to back on one
+    stream: the second output must equal the first, bit for bit, every time."""
+    import torch
+    a = ts.make_custom([65536], ratio=2, coff=1, d=512, pad_rows=0, seed=40)
+    dev = H.device_pack(a)
+    T2, d = a.total_comp, a.d
+    ref, _ = H.run_fwd(cuda_lib, a)
+    ape1 = torch.zeros((1, d), dtype=torch.float32, device="cuda")
+    cu1 = torch.tensor([0, T2], dtype=torch.int32, device="cuda")
+    x = torch.empty((T2, d), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((T2, d), dtype=torch.bfloat16, device="cuda")
+    nan = np.int16(np.uint16(H.BF16_NAN).view(np.int16))
+    for _ in range(5):
+        x.view(torch.int16).fill_(nan)
+        y.view(torch.int16).fill_(nan)
+        cuda_lib.csa_compressor_fwd(dev["kv"], dev["score"], dev["ape"], dev["cu_seqlens"], a.S,
+                                    a.ratio, a.coff, d, a.capacity, x, T2)
+        cuda_lib.csa_compressor_fwd(x, x, ape1, cu1, 1, 1, 1, d, T2, y, T2)
+        torch.cuda.synchronize()
+        assert (ts.bf16_tensor_bits(x) == ref).all()
+        assert (ts.bf16_tensor_bits(y) == ref).all()
