@@ -11,11 +11,16 @@ namespace csa {
 PoolKernel bwd_kernel_for(const Plan& pl) {
   if (pl.generic) return pool_generic_kernel<true>;
   if (pl.longk) {
+    const bool two = pl.coff == 2;
     switch (pl.pp) {
-      case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_BWD_GROUPS, true>);
-      case 2: return reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_BWD_GROUPS, true>);
-      case 4: return reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_BWD_GROUPS, true>);
-      case 8: return reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_BWD_GROUPS, true>);
+      case 1: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_BWD_GROUPS, 2, true>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_BWD_GROUPS, 1, true>);
+      case 2: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_BWD_GROUPS, 2, true>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_BWD_GROUPS, 1, true>);
+      case 4: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_BWD_GROUPS, 2, true>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_BWD_GROUPS, 1, true>);
+      case 8: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_BWD_GROUPS, 2, true>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_BWD_GROUPS, 1, true>);
       default: return nullptr;
     }
   }

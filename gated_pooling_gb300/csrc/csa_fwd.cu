@@ -11,11 +11,16 @@ namespace csa {
 PoolKernel fwd_kernel_for(const Plan& pl) {
   if (pl.generic) return pool_generic_kernel<false>;
   if (pl.longk) {
+    const bool two = pl.coff == 2;
     switch (pl.pp) {
-      case 1: return reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, false>);
-      case 2: return reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, false>);
-      case 4: return reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, false>);
-      case 8: return reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, false>);
+      case 1: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, 2, false>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, 1, false>);
+      case 2: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, 2, false>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, 1, false>);
+      case 4: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 2, false>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 1, false>);
+      case 8: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 2, false>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 1, false>);
       default: return nullptr;
     }
   }

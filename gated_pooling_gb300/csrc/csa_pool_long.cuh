@@ -76,7 +76,7 @@ __device__ __forceinline__ void sts_words2(void* p, uint32_t a, uint32_t b) {
 // 128-byte swizzle (tile base on a 1024-byte boundary): the chunk is stored at c ^ (y mod 8).
 __device__ __forceinline__ int swz(int y, int c) { return y * 128 + ((c ^ (y & 7)) << 4); }
 
-template <int PP, int NG, bool BWD>
+template <int PP, int NG, int COFF, bool BWD>
 __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     pool_long_kernel(const PoolParams p, const __grid_constant__ CUtensorMap tm_kv,
                      const __grid_constant__ CUtensorMap tm_sc,
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   pdl_trigger();  // the next kernel (the dAPE reduction, or the caller's) may launch
 
   const int r = p.r, d = p.d, C = p.C;
-  const bool two = p.coff == 2;
+  constexpr bool two = COFF == 2;
   const int col0 = blockIdx.x * kLongSlice;  // first column of the slice (in a half)
   const int g = blockIdx.y;
   const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
