@@ -35,11 +35,11 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) per backward call, from one ncu capture of this build (the
 # summaries are kept with the profiles): headline pack, pool kernel 108.28 MB read +
-# 47.03 MB write (the rest of its writes are still dirty in L2 when it ends), reduction
-# 2.50 MB read; long-window pack, pool kernel 135.66 + 82.83 MB, reduction 4.99 MB. It
+# 47.10 MB write (the rest of its writes are still dirty in L2 when it ends), reduction
+# 2.50 MB read; long-window pack, pool kernel 136.49 + 83.71 MB, reduction 4.99 MB. It
 # must be re-measured whenever a kernel changes.
-ROOFLINE_TRAFFIC = {"3x8192_d512": 108.280576e6 + 47.028992e6 + 2.500352e6,
-                    "long_r128_d512": 135.660544e6 + 82.827264e6 + 4.98944e6}
+ROOFLINE_TRAFFIC = {"3x8192_d512": 108.2816e6 + 47.097344e6 + 2.500352e6,
+                    "long_r128_d512": 136.485376e6 + 83.710464e6 + 4.989696e6}
 
 
 # ----------------------------------------------------------------------------------
