@@ -26,7 +26,10 @@
  *   - Every buffer belongs to the caller. The library allocates nothing, never
  *     synchronises, and never reads device memory from the host.
  *   - Work is enqueued on `stream` (NULL: the legacy default stream) of the current
- *     device; calls return as soon as it is enqueued.
+ *     device; calls return as soon as it is enqueued. The kernels are launched as
+ *     programmatic dependents of the stream's previous kernel: they may start while it
+ *     finishes, but read and write nothing before it has completed, so stream order
+ *     holds exactly as for ordinary launches (also inside CUDA graphs).
  *   - bf16 tensors are row-major and contiguous, fp32 tensors (ape, dape, workspace) too.
  *     Pointers need their natural alignment (2 bytes for bf16, 4 for fp32). The fast
  *     kernels run when d is a multiple of 8 and every pointer is 16-byte aligned; any
