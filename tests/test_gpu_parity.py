@@ -71,6 +71,17 @@ def small_packs():
         "many_segments": ts.make_custom(list(np.random.default_rng(1).integers(0, 12, 700)),
                                         ratio=4, coff=2, d=16, pad_rows=9, seed=16),
     }
+    # the maximum segment count: the block prefix alone takes 128 KB of shared memory, so
+    # every kernel runs with its smallest ring (the long-window shape falls back to the
+    # split kernel)
+    rng = np.random.default_rng(41)
+    packs["max_segments_r4c2_d16"] = ts.make_custom(list(rng.integers(0, 10, 16384)), ratio=4,
+                                                    coff=2, d=16, pad_rows=11, seed=42)
+    packs["max_segments_r2c2_d64"] = ts.make_custom(list(rng.integers(0, 10, 16384)), ratio=2,
+                                                    coff=2, d=64, pad_rows=11, seed=43)
+    packs["max_segments_r16c1_d128"] = ts.make_custom(list(rng.integers(0, 40, 16384)),
+                                                      ratio=16, coff=1, d=128, pad_rows=11,
+                                                      seed=44)
     lead = ts.make_custom([6, 9, 14], ratio=4, coff=2, d=16, pad_rows=3, seed=17)
     # same tensors with cu_seqlens starting at 6: rows 0..5 become padding, and the one
     # block of the dropped first segment leaves dout
