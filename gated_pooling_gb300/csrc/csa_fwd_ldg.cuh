@@ -2,9 +2,9 @@
 // positions (same operation as csa_pool_stream.cuh; "Megatron-LM PR #5984", commit "CSA:
 // add fused Compressor forward+backward CuTe-DSL kernels").
 //
-// The forward reads ~95% of its bytes. Streaming reads through bulk copies into shared
-// memory top out lower on GB300 than plain evict-first vector loads into registers with
-// enough of them in flight, so this variant keeps everything in registers: each thread
+// The forward reads ~95% of its bytes. For short windows and narrow rows the bulk-copy
+// pipeline's per-row and start-up costs dominate (a stage per row of a few KB), so this
+// variant keeps everything in registers: each thread
 // owns one chunk of 4 columns of a row (both halves at coff=2) and loads, per row, the
 // 2*W 8-byte pieces of its window (kv and score) itself. The loads of the thread's next
 // PF rows are in flight while a row is computed (a ring of PF + 1 register buffers; PF is

@@ -1,5 +1,7 @@
-// csa_pool.cuh -- the pooling kernel of the GB300 CSA/HCA compressor, forward and
-// backward, and its launch planning.
+// csa_pool.cuh -- the general (split-window) pooling kernel of the GB300 CSA/HCA
+// compressor, forward and backward, and the launch geometry of every pooling kernel (the
+// specialised ones are csa_pool_stream.cuh, csa_fwd_ldg.cuh, csa_pool_long.cuh and
+// csa_pool_generic.cuh; csa_api.cu picks one per call).
 //
 // Operation ("Megatron-LM PR #5984", commit "CSA: add fused Compressor
 // forward+backward CuTe-DSL kernels"): per output row (one block of ratio tokens of

@@ -1,6 +1,7 @@
 // csa_pool_stream.cuh -- block-streaming pooling kernel for windows of up to 8 positions
-// (the ratio=4 and ratio=2 coff=2 packs of the pages, and coff=1 up to ratio=8), forward
-// and backward.
+// (ratio 1, 2, 4 at coff=2 and up to ratio 8 at coff=1): the backward of all of them and
+// the forward of 8-position windows on wide rows (the headline ratio=4 coff=2 d=512
+// pack; shorter windows and narrow rows go forward through csa_fwd_ldg.cuh).
 //
 // Same operation and zero ownership as pool_kernel (csa_pool.cuh). One CTA per SM owns a
 // contiguous range of output rows [o0, o1). Output row o is block b of segment s; its R
@@ -11,9 +12,11 @@
 // the stage's `full` mbarrier. The window of row o is the left half of stage o-1
 // (previous block, coff=2) and the right half of stage o (own block; the whole stage at
 // coff=1), so every consumed byte crosses HBM once. A stage is released (`empty`
-// mbarrier) once rows o and o+1 have read it. The block before o0 (read by row o0 when it
-// is not a segment's first block) is fetched once, left half only, into a buffer laid
-// out like a stage.
+// mbarrier) once rows o and o+1 have read it; ring slots and phases are running counters.
+// The block before o0 (read by row o0 when it is not a segment's first block) is fetched
+// once, left half only, into a buffer laid out like a stage, its row copies issued by the
+// producer warp's lanes together. The mbarriers are set up, one per thread, before the
+// index map is read.
 //
 // Consumers (NC threads): a thread owns one chunk of VEC columns of a row, the same
 // chunk in both halves; NC/(d/VEC) rows are computed at once (row j -> row slot j mod
