@@ -396,16 +396,24 @@ __global__ void __launch_bounds__(kThreads, 2) pool_kernel(const PoolParams p) {
       for (int i = 0; i < PP; ++i)
 #pragma unroll
         for (int c = 0; c < VEC; ++c) red[(i * VEC + c) * kThreads + tid] = acc[i][c];
+      // slots added pairwise in a fixed tree (slot q absorbs slot q + h, h = the powers
+      // of two below the slot count, largest first): each thread adds into its own entries
+      const int ns = p.slots;
+      int h = 1;
+      while (2 * h < ns) h *= 2;
+      for (; h >= 1; h /= 2) {
+        __syncthreads();
+        if (slot < h && slot + h < ns)
+#pragma unroll
+          for (int iv = 0; iv < PP * VEC; ++iv)
+            red[iv * kThreads + tid] += red[iv * kThreads + tid + h * tps];
+      }
       __syncthreads();
       if (slot == 0) {
 #pragma unroll
         for (int i = 0; i < PP; ++i)
 #pragma unroll
-          for (int c = 0; c < VEC; ++c) {
-            float sum = red[(i * VEC + c) * kThreads + tid];
-            for (int sl = 1; sl < p.slots; ++sl) sum += red[(i * VEC + c) * kThreads + sl * tps + tid];
-            acc[i][c] = sum;
-          }
+          for (int c = 0; c < VEC; ++c) acc[i][c] = red[(i * VEC + c) * kThreads + tid];
       }
     }
     if (slot == 0 && col_ok) {

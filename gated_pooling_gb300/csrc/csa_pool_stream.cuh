@@ -410,6 +410,20 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
           red[(i * VEC + 2 * q + 1) * NC + tid] = f2_hi(acc[i][q]);
         }
     }
+    // the row slots of every (position, column) added pairwise in a fixed tree (slot q
+    // absorbs slot q + h, h = the powers of two below the slot count, largest first; each
+    // thread adds into its own entries): log2(slots) short steps instead of a serial sum
+    // over the slots (narrow rows have up to ~60 of them)
+    const int ns = p.slots;
+    int h = 1;
+    while (2 * h < ns) h *= 2;
+    const int rs = tid / V;  // this thread's row slot (its column of red is tid)
+    for (; ns > 1 && h >= 1; h /= 2) {
+      __syncthreads();
+      if (tid < NC && rs < h && rs + h < ns)
+#pragma unroll
+        for (int iv = 0; iv < W * VEC; ++iv) red[iv * NC + tid] += red[iv * NC + tid + h * V];
+    }
     __syncthreads();
     if (tid < V) {
       const int c0 = tid * VEC;
@@ -418,10 +432,7 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
       for (int i = 0; i < W; ++i) {
         float sum[VEC];
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) sum[c] = 0.f;
-        for (int q = 0; q < p.slots; ++q)
-#pragma unroll
-          for (int c = 0; c < VEC; ++c) sum[c] += red[(i * VEC + c) * NC + q * V + tid];
+        for (int c = 0; c < VEC; ++c) sum[c] = red[(i * VEC + c) * NC + tid];
         const bool prev = TWO && i < R;
         const int arow = (TWO && !prev) ? i - R : i;
         const int col = ((TWO && !prev) ? d : 0) + c0;
