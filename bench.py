@@ -34,11 +34,11 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) per backward call, from one ncu capture of this build (the
-# summaries are kept with the profiles): headline pack, pool kernel 108.28 MB read +
-# 47.32 MB write (the rest of its writes are still dirty in L2 when it ends), reduction
+# summaries are kept with the profiles): headline pack, pool kernel 108.27 MB read +
+# 46.71 MB write (the rest of its writes are still dirty in L2 when it ends), reduction
 # 2.50 MB read; long-window pack, pool kernel 136.49 + 83.71 MB, reduction 4.99 MB. It
 # must be re-measured whenever a kernel changes.
-ROOFLINE_TRAFFIC = {"3x8192_d512": 108.281088e6 + 47.324416e6 + 2.500608e6,
+ROOFLINE_TRAFFIC = {"3x8192_d512": 108.265216e6 + 46.7072e6 + 2.500352e6,
                     "long_r128_d512": 136.485376e6 + 83.710464e6 + 4.989696e6}
 
 
