@@ -63,6 +63,12 @@ def small_packs():
         "g_d9_r16c2": ts.make_custom([70, 33, 15], ratio=16, coff=2, d=9, pad_rows=2, seed=34),
         "g_d201_r128c2": ts.make_custom([400, 256, 100], ratio=128, coff=2, d=201, pad_rows=1,
                                         seed=35),
+        # the largest window accepted (coff * ratio = 2048 positions, split kernel: 256
+        # position groups merged through shared memory)
+        "r1024c2_d16": ts.make_custom([2100, 1024, 3000, 900], ratio=1024, coff=2, d=16,
+                                      pad_rows=5, seed=36, score_scale=4.0),
+        "r2048c1_d8": ts.make_custom([4200, 2047, 2048], ratio=2048, coff=1, d=8, pad_rows=3,
+                                     seed=37),
         "r128c2_split_d32": ts.make_custom([400, 128, 127], ratio=128, coff=2, d=32, pad_rows=3,
                                            seed=12),
         "all_short": ts.make_custom([1, 2, 3], ratio=4, coff=2, d=8, pad_rows=2, seed=13),
