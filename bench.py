@@ -7,10 +7,17 @@ the full dKV/dScore writes, ape and dAPE; workspace traffic is not counted).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
-N > 1 runs under torch.distributed.run: each rank runs its own replica of the pack on
-its own GPU (the pooling has no cross-pack exchange), timing is the max over ranks, and
-the value is the bytes of all ranks over that time. Rank 0 prints one JSON line.
---impl reference times the fp64 CPU oracle on the host cores instead (rank 0 only).
+Two timed passes of K steps each, both reported; `value` is the lower throughput:
+  * flushed: before every step (outside the events) L2 is flushed, then one fwd+bwd is
+    timed with events on its boundaries;
+  * steady: K back-to-back fwd+bwd steps between two events, rotating over enough full
+    buffer sets (inputs and outputs) that their total exceeds twice the L2 size, with no
+    flush, so every step also pays the write-back of the previous step's gradients.
+N > 1 runs one replica of the pack per GPU (the pooling has no cross-pack exchange):
+under torch.distributed.run, or, when started without it, by relaunching itself under
+it with N processes. Timing is the max over ranks, and the value is the bytes of all
+ranks over that time. Rank 0 prints one JSON line.
+--impl reference times the fp64 CPU oracle on all host cores instead (rank 0 only).
 """
 from __future__ import annotations
 
@@ -33,18 +40,16 @@ METRIC = "fwd+bwd µs and achieved HBM GB/s (% of GB300 roofline) per THD pack"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-# DRAM bytes (read + write) per backward call, from one ncu capture of this build (the
-# summaries are kept with the profiles): headline pack, pool kernel 108.27 MB read +
-# 46.71 MB write (the rest of its writes are still dirty in L2 when it ends), reduction
-# 2.50 MB read; long-window pack, pool kernel 136.49 + 83.71 MB, reduction 4.99 MB. It
-# must be re-measured whenever a kernel changes.
 # The pages' own fwd + bwd times for the packs they measure (forward kernel after
 # vectorisation + backward region, nsys kernel time, on B200 -- another machine: context,
 # not the target). vs_baseline = our GB/s / (the same algorithmic bytes / that time).
 PAGE_FWD_BWD_US = {"1x8192_d128": 4.5 + 12.8, "3x8192_d128": 10.0 + 22.2,
                    "1x8192_d512": 12.4 + 22.8, "3x8192_d512": 35.0 + 66.0}
-ROOFLINE_TRAFFIC = {"3x8192_d512": 108.265216e6 + 46.7072e6 + 2.500352e6,
-                    "long_r128_d512": 136.485376e6 + 83.710464e6 + 4.989696e6}
+# DRAM bytes per backward call (pool kernel + reduction), from one ncu capture of the
+# current kernels (the summaries are kept with the profiles): DRAM reads plus the bytes
+# the kernels write into L2 (all of which reach DRAM). Re-measured whenever a kernel
+# changes; absent (null) until then.
+ROOFLINE_TRAFFIC = {}
 
 
 # ----------------------------------------------------------------------------------
@@ -160,20 +165,34 @@ def run_ours(args, rank, world, local_rank):
     gp.load()
     pack = ts.make_pack(args.config)
     fwd_b, bwd_b = algorithmic_bytes(pack)
-    t = ts.to_torch(pack, dev)
     S, r, coff, d, cap, TC, C = (pack.S, pack.ratio, pack.coff, pack.d, pack.capacity,
                                  pack.total_comp, pack.C)
-    out = torch.empty((TC, d), dtype=torch.bfloat16, device=dev)
-    dkv = torch.empty((cap, C), dtype=torch.bfloat16, device=dev)
-    dsc = torch.empty((cap, C), dtype=torch.bfloat16, device=dev)
-    dape = torch.empty((r, C), dtype=torch.float32, device=dev)
     wsb = gp.csa_compressor_bwd_workspace_bytes(S, r, coff, d, cap, TC)
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
+
+    def buffer_set(inputs):
+        return {"in": inputs,
+                "out": torch.empty((TC, d), dtype=torch.bfloat16, device=dev),
+                "dkv": torch.empty((cap, C), dtype=torch.bfloat16, device=dev),
+                "dsc": torch.empty((cap, C), dtype=torch.bfloat16, device=dev),
+                "dape": torch.empty((r, C), dtype=torch.float32, device=dev),
+                "ws": torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)}
+
+    def set_bytes(bs):
+        ts_ = list(bs["in"].values()) + [bs[k] for k in ("out", "dkv", "dsc", "dape", "ws")]
+        return sum(x.numel() * x.element_size() for x in ts_)
+
+    # the steady pass rotates over enough full buffer sets (inputs and outputs) that their
+    # total is more than twice the L2 size: no step finds its data in L2
+    base = buffer_set(ts.to_torch(pack, dev))
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (132 << 20))
+    n_sets = max(args.rotate, -(-2 * l2 // set_bytes(base)))
+    sets = [base] + [buffer_set({k: v.clone() for k, v in base["in"].items()})
+                     for _ in range(n_sets - 1)]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def flush_l2():
         # write a buffer larger than L2, then read another one: L2 ends up holding clean
@@ -181,24 +200,28 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         flush_rd.sum()
 
-    def fwd():
+    def fwd(bs, e=err, strm=sp):
+        t = bs["in"]
         gp.csa_compressor_fwd(t["kv"], t["score"], t["ape"], t["cu_seqlens"], S, r, coff, d,
-                              cap, out, TC, err, stream=sp)
+                              cap, bs["out"], TC, e, stream=strm)
 
-    def bwd():
+    def bwd(bs, e=err, strm=sp):
+        t = bs["in"]
         gp.csa_compressor_bwd(t["kv"], t["score"], t["ape"], t["cu_seqlens"], t["dout"], S, r,
-                              coff, d, cap, TC, dkv, dsc, dape, 0, ws, wsb, err, stream=sp)
+                              coff, d, cap, TC, bs["dkv"], bs["dsc"], bs["dape"], 0, bs["ws"],
+                              wsb, e, stream=strm)
 
-    for _ in range(args.warmup):
+    for k in range(max(args.warmup, n_sets)):
         flush_l2()
-        fwd()
-        bwd()
+        fwd(sets[k % n_sets])
+        bwd(sets[k % n_sets])
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error {int(err.item())}")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    def new_events(n):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
     props = torch.cuda.get_device_properties(dev)
     gpu_id = str(getattr(props, "uuid", local_rank))
     if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
@@ -206,39 +229,55 @@ def run_ours(args, rank, world, local_rank):
     sampler = ClockSampler(gpu_id)
     if rank == 0:
         sampler.start()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    # the K timed steps: events on the step's boundaries only, so the backward's launch may
-    # overlap the forward's tail as it does when a user issues the two calls back to back
+
+    def bracket():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # pass 1, flushed: the K timed steps with L2 flushed before each (outside the events),
+    # events on each step's boundaries only, so the backward's launch may overlap the
+    # forward's tail as it does when a user issues the two calls back to back
+    sev = [new_events(2) for _ in range(args.steps)]
+    bracket()
     for k in range(args.steps):
-        flush_l2()                      # L2 flush, outside the events
+        flush_l2()
         sev[k][0].record(stream)
-        fwd()
-        bwd()
+        fwd(base)
+        bwd(base)
         sev[k][1].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    # the per-call split (and the roofline's backward-call time): the same K steps with an
+    bracket()
+    # pass 2, steady: K back-to-back steps over the rotated buffer sets, no flush
+    st0, st1 = new_events(2)
+    bracket()
+    st0.record(stream)
+    for k in range(args.steps):
+        fwd(sets[k % n_sets])
+        bwd(sets[k % n_sets])
+    st1.record(stream)
+    bracket()
+    # the per-call split (and the roofline's backward-call time): K flushed steps with an
     # event between the two calls, which keeps the backward from starting early
+    ev = [new_events(3) for _ in range(args.steps)]
     for k in range(args.steps):
         flush_l2()
         ev[k][0].record(stream)
-        fwd()
+        fwd(base)
         ev[k][1].record(stream)
-        bwd()
+        bwd(base)
         ev[k][2].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    bracket()
     clocks = sampler.stop() if rank == 0 else None
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())}")
     step_ms = [sev[k][0].elapsed_time(sev[k][1]) for k in range(args.steps)]
     fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
-    total_ms, fwd_total, bwd_total = max_over_ranks(
-        [sum(step_ms), sum(fwd_ms), sum(bwd_ms)], device=dev)
-    ms_step = total_ms / args.steps
+    total_ms, steady_total, fwd_total, bwd_total = max_over_ranks(
+        [sum(step_ms), st0.elapsed_time(st1), sum(fwd_ms), sum(bwd_ms)], device=dev)
+    flushed_ms = total_ms / args.steps
+    steady_ms = steady_total / args.steps
+    ms_step = max(flushed_ms, steady_ms)  # the lower throughput is the headline
     fwd_us = fwd_total / args.steps * 1e3
     bwd_us = bwd_total / args.steps * 1e3
     value = whole_job_gbs(world, fwd_b + bwd_b, ms_step)
@@ -251,13 +290,10 @@ def run_ours(args, rank, world, local_rank):
         side.wait_stream(stream)
         with torch.cuda.stream(side):
             with torch.cuda.graph(g, stream=side):
-                gp.csa_compressor_fwd(t["kv"], t["score"], t["ape"], t["cu_seqlens"], S, r, coff,
-                                      d, cap, out, TC, err)
-                gp.csa_compressor_bwd(t["kv"], t["score"], t["ape"], t["cu_seqlens"], t["dout"],
-                                      S, r, coff, d, cap, TC, dkv, dsc, dape, 0, ws, wsb, err)
+                fwd(base, strm=None)
+                bwd(base, strm=None)
         stream.wait_stream(side)
-        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(min(args.steps, 200))]
+        gev = [new_events(2) for _ in range(min(args.steps, 200))]
         for a, b in gev:
             flush_l2()
             a.record(stream)
@@ -267,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
         graph_us = round(1e3 * sum(a.elapsed_time(b) for a, b in gev) / len(gev), 2)
 
     # end to end through the public API with host buffers (copies inside the region)
-    e2e = run_e2e(args, pack, t, dev, fwd_b + bwd_b, wsb) if rank == 0 else None
+    e2e = run_e2e(args, pack, base["in"], dev, fwd_b + bwd_b, wsb) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
     if rank != 0:
@@ -283,6 +319,7 @@ def run_ours(args, rank, world, local_rank):
                     "source": f"the pages' fwd + bwd kernel times ({PAGE_FWD_BWD_US[args.config]:.1f} "
                               "us, nsys, B200: another machine, context only) over the same "
                               "algorithmic bytes"}
+    per_gpu = lambda ms: (fwd_b + bwd_b) / (ms * 1e-3) / 1e9
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -290,8 +327,18 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": workload_name(pack), "ratio": r, "coff": coff, "d": d, "S": S,
                    "capacity": cap, "total_comp": TC,
-                   "l2": f"flushed before every step outside the timed events ({L2_FLUSH_BYTES >> 20} MiB write, then a {L2_FLUSH_BYTES >> 20} MiB read)",
+                   "l2": (f"value = the slower of two passes: (flushed) L2 flushed before every "
+                          f"step outside the timed events ({L2_FLUSH_BYTES >> 20} MiB write, then "
+                          f"a {L2_FLUSH_BYTES >> 20} MiB read); (steady) back-to-back steps "
+                          f"rotating over {n_sets} full buffer sets of "
+                          f"{set_bytes(base) / 1e6:.1f} MB (> 2x the {l2 >> 20} MiB L2), no "
+                          f"flush"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "flushed": {"us_per_step": round(flushed_ms * 1e3, 2),
+                    "gbs_per_gpu": round(per_gpu(flushed_ms), 1)},
+        "steady": {"us_per_step": round(steady_ms * 1e3, 2),
+                   "gbs_per_gpu": round(per_gpu(steady_ms), 1), "buffer_sets": n_sets,
+                   "set_bytes": set_bytes(base)},
         "fwd_us": round(fwd_us, 2), "bwd_us": round(bwd_us, 2),
         "fwd_plus_bwd_calls_us": round(fwd_us + bwd_us, 2),
         "graph_fwd_bwd_us": graph_us,
@@ -307,7 +354,9 @@ def run_ours(args, rank, world, local_rank):
                      "achieved": round(bwd_gbs, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(bwd_gbs / peak, 4),
                      "traffic": ROOFLINE_TRAFFIC.get(args.config)},
-        "e2e": e2e, "clocks": clocks, "gpu_launches": 3 * args.steps,
+        "e2e": e2e, "clocks": clocks,
+        # our kernels per timed pass: forward, pooling backward, dAPE reduction per step
+        "gpu_launches": 3 * args.steps,
         "baseline": baseline,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -410,28 +459,49 @@ def sample_pack(pack, tokens: int):
                    pack.score[c0:c0 + tokens], pack.ape, pack.dout[:n])
 
 
-def oracle_step_seconds(sp):
+def oracle_step_seconds(sp, threads: int = 1):
+    """One fwd + bwd pass of the oracle: the single-thread entry points, or the
+    multi-thread drivers over `threads` host threads."""
     import oracle
     t0 = time.perf_counter()
-    oracle.fwd_pack(sp)
-    oracle.bwd_pack(sp)
+    if threads == 1:
+        oracle.fwd_pack(sp)
+        oracle.bwd_pack(sp)
+    else:
+        oracle.fwd_threads(sp, threads)
+        oracle.bwd_threads(sp, threads)
     return time.perf_counter() - t0
 
 
 def cpu_baseline(pack, budget_s=12.0):
-    """The oracle as it stands, single-threaded, on a bounded sample of the pack."""
-    tokens = min(int(pack.cu_seqlens[1]) - int(pack.cu_seqlens[0]), 8192)
-    sp = sample_pack(pack, tokens)
-    fb, bb = algorithmic_bytes(sp)
+    """The oracle as it stands, timed on this host: on all cores (std::thread over output
+    rows) on the whole pack, and single-threaded on a bounded sample (the first 8192
+    tokens of segment 0). `value` is the all-core figure."""
+    import oracle
+    cores = oracle.hardware_threads()
+    fb, bb = algorithmic_bytes(pack)
     times = []
-    t_end = time.perf_counter() + budget_s
-    while not times or (time.perf_counter() < t_end and len(times) < 20):
-        times.append(oracle_step_seconds(sp))
-    sec = statistics.median(times)
-    return {"value": round((fb + bb) / sec / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {sp.capacity} tokens of segment 0 ({sp.total_comp} output rows), "
-                      f"fwd+bwd x{len(times)}, median {sec:.3f} s per pass",
-            "sec_per_pass": round(sec, 4)}
+    t_end = time.perf_counter() + budget_s / 2
+    while not times or (time.perf_counter() < t_end and len(times) < 10):
+        times.append(oracle_step_seconds(pack, cores))
+    sec_mt = statistics.median(times)
+    sp = sample_pack(pack, min(int(pack.cu_seqlens[1]) - int(pack.cu_seqlens[0]), 8192))
+    sfb, sbb = algorithmic_bytes(sp)
+    stimes = []
+    t_end = time.perf_counter() + budget_s / 2
+    while not stimes or (time.perf_counter() < t_end and len(stimes) < 10):
+        stimes.append(oracle_step_seconds(sp))
+    sec_st = statistics.median(stimes)
+    return {"value": round((fb + bb) / sec_mt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"the whole pack, fwd+bwd on {cores} host threads (output-row ranges), "
+                      f"x{len(times)}, median {sec_mt:.3f} s per pass",
+            "sec_per_pass": round(sec_mt, 4),
+            "single_thread": {"value": round((sfb + sbb) / sec_st / 1e9, 4), "unit": "GB/s",
+                              "cores": 1,
+                              "sample": f"first {sp.capacity} tokens of segment 0 "
+                                        f"({sp.total_comp} output rows), x{len(stimes)}, "
+                                        f"median {sec_st:.3f} s per pass"}}
 
 
 def run_reference(args, rank):
@@ -439,22 +509,26 @@ def run_reference(args, rank):
         return None
     import oracle
     oracle.build()
+    cores = oracle.hardware_threads()
     pack = ts.make_pack(args.config)
-    # size the per-step sample so the whole run stays within about two minutes
-    probe = sample_pack(pack, 64 * pack.ratio)
-    per_tok = oracle_step_seconds(probe) / probe.capacity
+    # each step is the whole pack on all host cores when that keeps the run within about
+    # two minutes, else the first tokens of segment 0 that do
     budget = 120.0 / max(1, args.steps + args.warmup)
-    full = int(pack.cu_seqlens[1]) - int(pack.cu_seqlens[0])
-    tokens = int(max(pack.ratio, min(full, budget / max(per_tok, 1e-9))))
-    sp = sample_pack(pack, tokens)
+    probe = sample_pack(pack, 256 * pack.ratio)
+    per_tok = oracle_step_seconds(probe, cores) / probe.capacity
+    if per_tok * pack.capacity <= budget:
+        sp, desc_sample = pack, "the whole pack"
+    else:
+        full = int(pack.cu_seqlens[1]) - int(pack.cu_seqlens[0])
+        sp = sample_pack(pack, int(max(pack.ratio, min(full, budget / max(per_tok, 1e-9)))))
+        desc_sample = f"the first {sp.capacity} tokens of segment 0 ({sp.total_comp} output rows)"
     fb, bb = algorithmic_bytes(sp)
     for _ in range(args.warmup):
-        oracle_step_seconds(sp)
-    times = [oracle_step_seconds(sp) for _ in range(args.steps)]
+        oracle_step_seconds(sp, cores)
+    times = [oracle_step_seconds(sp, cores) for _ in range(args.steps)]
     ms = 1e3 * sum(times) / len(times)
     value = (fb + bb) / (ms * 1e-3) / 1e9
-    desc = (f"fp64 oracle, single thread, on the first {sp.capacity} tokens of segment 0 "
-            f"({sp.total_comp} output rows) per step")
+    desc = f"fp64 oracle on {cores} host threads (output-row ranges), {desc_sample} per step"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
@@ -462,10 +536,29 @@ def run_reference(args, rank):
             "config": {"workload": workload_name(pack), "ratio": pack.ratio, "coff": pack.coff,
                        "d": pack.d, "S": pack.S, "capacity": pack.capacity,
                        "total_comp": pack.total_comp},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------------
+# Launch
+# ----------------------------------------------------------------------------------
+
+def replica_command(script, argv, nproc: int, port: int):
+    """The command that runs `script argv` as `nproc` ranks of one node under
+    torch.distributed.run, rendezvous on 127.0.0.1:`port`."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={nproc}", "--master-addr", "127.0.0.1",
+            f"--master-port={port}", script, *argv]
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
 
 
 def main():
@@ -475,6 +568,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=ts.HEADLINE, choices=sorted(ts.SPECS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--rotate", type=int, default=3,
+                    help="minimum buffer sets the steady pass rotates over")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -482,6 +577,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.rotate < 3:
+        ap.error("--rotate must be at least 3")
+
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1 and args.impl == "ours":
+        # one replica per GPU: relaunch under torch.distributed.run with N ranks
+        cmd = replica_command(os.path.abspath(__file__), sys.argv[1:], args.gpus, free_port())
+        sys.exit(subprocess.call(cmd))
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -20,11 +20,13 @@ from . import build as _build
 LIB_PATH = _build.LIB
 _lib: Optional[ctypes.CDLL] = None
 
-CSA_OK, CSA_ERR_INVALID_VALUE, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA = 0, 1, 2, 3
-CSA_DEVERR_CU_SEQLENS, CSA_DEVERR_OUT_ROWS = 1, 2
+CSA_OK, CSA_ERR_INVALID_VALUE, CSA_ERR_UNSUPPORTED, CSA_ERR_WORKSPACE, CSA_ERR_CUDA = 0, 1, 2, 3, 4
+CSA_DEVERR_CU_SEQLENS, CSA_DEVERR_OUT_ROWS, CSA_DEVERR_TIMEOUT = 1, 2, 3
+CSA_TEST_MIN_WAIT_CYCLES = 1000000
 EXPORTED = ("csa_status_string", "csa_last_error_string", "csa_compressor_total_comp", "csa_compressor_fwd",
             "csa_compressor_bwd_workspace_bytes", "csa_compressor_bwd",
-            "csa_compressor_bwd_noalloc", "csa_compressor_map_blocks")
+            "csa_compressor_bwd_noalloc", "csa_compressor_test_hooks",
+            "csa_compressor_map_blocks")
 
 
 class CsaError(RuntimeError):
@@ -63,6 +65,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_compressor_bwd_noalloc.restype = ctypes.c_int
     lib.csa_compressor_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i64,
                                                vp, vp, vp, i32, vp, vp]
+    lib.csa_compressor_test_hooks.restype = ctypes.c_int
+    lib.csa_compressor_test_hooks.argtypes = [i64, i32]
     lib.csa_compressor_map_blocks.restype = ctypes.c_int
     lib.csa_compressor_map_blocks.argtypes = [vp, i32, i32, i64, i64, vp, vp, vp]
     if path == LIB_PATH:
@@ -144,6 +148,13 @@ def csa_compressor_bwd_noalloc(kv, score, ape, cu_seqlens, dout, S: int, ratio: 
                                              _ptr(dkv), _ptr(dscore), _ptr(dape),
                                              int(accumulate_dape), _ptr(dev_error),
                                              _stream(stream)), "csa_compressor_bwd_noalloc")
+
+
+def csa_compressor_test_hooks(wait_cycles: int, withhold_row: int) -> None:
+    """Test hook: pipeline wait bound (0 = default) and the row whose copies the first
+    CTA's producer withholds (-1 = off), for every later call."""
+    _check(load().csa_compressor_test_hooks(int(wait_cycles), int(withhold_row)),
+           "csa_compressor_test_hooks")
 
 
 def csa_compressor_map_blocks(cu_seqlens, S: int, ratio: int, capacity: int, out_rows: int,

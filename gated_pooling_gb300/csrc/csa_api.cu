@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <climits>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -28,6 +29,9 @@ std::vector<OccEntry> g_occ;
 std::vector<int> g_sms;
 std::vector<std::pair<int, const void*>> g_attr_set;
 thread_local cudaError_t t_last_error = cudaSuccess;
+// Test hook state (csa_compressor_test_hooks): the pipeline wait bound and the withheld row.
+std::atomic<long long> g_wait_cycles{kWaitCycles};
+std::atomic<int> g_withhold_row{-1};
 
 // Records a failing CUDA call for csa_last_error_string() and passes the code on.
 cudaError_t note(cudaError_t e) {
@@ -138,6 +142,15 @@ csa_status_t check_sizes(int32_t S, int32_t ratio, int32_t coff, int32_t d, int6
 
 static_assert(kGenericMaxWindow == CSA_MAX_GENERIC_WINDOW, "generic window limit");
 
+// Backward workspace: the fp32 dAPE partials [R, ratio, coff*d], then (at the next 16-byte
+// boundary) the call's status word that the pooling kernel writes and the reduction reads.
+size_t partial_bytes(const Plan& pl, int32_t ratio, int32_t coff, int32_t d) {
+  return (static_cast<size_t>(pl.R) * ratio * coff * d * sizeof(float) + 15) & ~static_cast<size_t>(15);
+}
+size_t workspace_need(const Plan& pl, int32_t ratio, int32_t coff, int32_t d) {
+  return partial_bytes(pl, ratio, coff, d) + 16;
+}
+
 // Plan plus the device-dependent row-group count R. `fast`: d % 8 == 0 and every pointer
 // 16-byte aligned (the vector kernels); otherwise the generic scalar kernel.
 csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t d,
@@ -208,6 +221,8 @@ PoolParams base_params(const Plan& pl, const void* kv, const void* score, const 
   p.ring_off = pl.ring_off;
   p.bar_off = pl.bar_off;
   p.box_rows = pl.box_rows;
+  p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
+  p.withhold_row = g_withhold_row.load(std::memory_order_relaxed);
   return p;
 }
 
@@ -276,12 +291,15 @@ __device__ __forceinline__ void neumaier_add(float& s, float& c, float x) {
 // may start early and waits for that grid's results.
 constexpr int kReduceCols = 32;
 constexpr int kReduceBatch = 12;  // partials a thread has in flight at once
+// A non-zero status word (the pooling kernel found cu_seqlens or out_rows invalid) leaves
+// dAPE untouched.
 template <int SPLIT>
 __global__ void __launch_bounds__(kReduceCols * SPLIT)
     dape_reduce_kernel(const float* __restrict__ partial, int R, int n, float* __restrict__ dape,
-                       int accumulate) {
+                       int accumulate, const int32_t* __restrict__ status) {
   constexpr int kReduceSplit = SPLIT;
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return;
   __shared__ float s_sum[kReduceSplit][kReduceCols];
   __shared__ float s_cmp[kReduceSplit][kReduceCols];
   const int lane = threadIdx.x % kReduceCols;
@@ -360,8 +378,9 @@ extern "C" {
 const char* csa_status_string(int status) {
   switch (status) {
     case CSA_OK: return "CSA_OK";
-    case CSA_ERR_INVALID_VALUE: return "CSA_ERR_INVALID_VALUE: null, negative, misaligned or too small argument";
+    case CSA_ERR_INVALID_VALUE: return "CSA_ERR_INVALID_VALUE: null, negative or misaligned argument";
     case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: coff not in {1,2}, or a size limit exceeded";
+    case CSA_ERR_WORKSPACE: return "CSA_ERR_WORKSPACE: workspace missing or smaller than csa_compressor_bwd_workspace_bytes";
     case CSA_ERR_CUDA: return "CSA_ERR_CUDA: a CUDA runtime call or kernel launch failed";
     default: return "unknown csa status";
   }
@@ -416,7 +435,7 @@ size_t csa_compressor_bwd_workspace_bytes(int32_t S, int32_t ratio, int32_t coff
     Plan pl;
     PoolKernel k;
     if (make_plan(true, S, ratio, coff, d, out_rows, fast != 0, &pl, &k) != CSA_OK) continue;
-    need = std::max(need, static_cast<size_t>(pl.R) * ratio * coff * d * sizeof(float));
+    need = std::max(need, workspace_need(pl, ratio, coff, d));
   }
   return need;
 }
@@ -442,17 +461,22 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
                     aligned16(workspace);
   if (!fast && coff * ratio > CSA_MAX_GENERIC_WINDOW) return CSA_ERR_UNSUPPORTED;
   Plan pl;
+  pl.R = 1;  // no plan has fewer row groups: smaller workspaces are rejected before planning
+  if (workspace == nullptr || workspace_bytes < workspace_need(pl, ratio, coff, d))
+    return CSA_ERR_WORKSPACE;
   PoolKernel k;
   st = make_plan(true, S, ratio, coff, d, out_rows, fast, &pl, &k);
   if (st != CSA_OK) return st;
-  const size_t need = static_cast<size_t>(pl.R) * ratio * coff * d * sizeof(float);
-  if (workspace == nullptr || workspace_bytes < need) return CSA_ERR_INVALID_VALUE;
+  const size_t need = workspace_need(pl, ratio, coff, d);
+  if (workspace == nullptr || workspace_bytes < need) return CSA_ERR_WORKSPACE;
   PoolParams p = base_params(pl, kv, score, ape, cu_seqlens, S, ratio, coff, d, capacity,
                              out_rows, dev_error);
   p.dout = static_cast<const uint16_t*>(dout);
   p.dkv = static_cast<uint16_t*>(dkv);
   p.dscore = static_cast<uint16_t*>(dscore);
   p.partial = static_cast<float*>(workspace);
+  p.status = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) +
+                                        partial_bytes(pl, ratio, coff, d));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   st = launch(k, pl, p, s);
   if (st != CSA_OK) return st;
@@ -460,7 +484,8 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
   int n = ratio * coff * d;
   int R = pl.R;
   int acc = accumulate_dape != 0;
-  void* rargs[] = {&part, &R, &n, &dape, &acc};
+  const int32_t* status = p.status;
+  void* rargs[] = {&part, &R, &n, &dape, &acc, &status};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -483,6 +508,15 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
   const cudaError_t e =
       note(cudaLaunchKernelExC(&cfg, rk, rargs));
   return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+csa_status_t csa_compressor_test_hooks(int64_t wait_cycles, int32_t withhold_row) {
+  if (wait_cycles < 0 || (wait_cycles > 0 && wait_cycles < CSA_TEST_MIN_WAIT_CYCLES) ||
+      wait_cycles > kWaitCycles)
+    return CSA_ERR_INVALID_VALUE;
+  g_wait_cycles.store(wait_cycles == 0 ? kWaitCycles : wait_cycles, std::memory_order_relaxed);
+  g_withhold_row.store(withhold_row < 0 ? -1 : withhold_row, std::memory_order_relaxed);
+  return CSA_OK;
 }
 
 csa_status_t csa_compressor_map_blocks(const int32_t* cu_seqlens, int32_t S, int32_t ratio,

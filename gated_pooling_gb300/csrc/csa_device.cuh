@@ -387,14 +387,18 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for the phase with `parity` of `bar` to complete, giving up after about
-// kWaitCycles SM clock cycles (returns false then). No wait in this library is unbounded.
+// Waits for the phase with `parity` of `bar` to complete, giving up after about `limit`
+// SM clock cycles (returns false then). No wait in this library is unbounded. The
+// pipeline waits take the call's limit (PoolParams::wait_cycles, kWaitCycles unless a
+// test shortened it); the waits that let a stopping CTA's own copies land before it
+// exits always take kWaitCycles.
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at GB300 clocks
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 

@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
 
   const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
+  publish_status(p, TC);
   if (TC < 0) return;
   pdl_trigger();  // the next kernel of the stream may launch
 

@@ -54,7 +54,11 @@ struct PoolParams {
   uint16_t* dkv;          // bf16 [capacity, C]   (backward)
   uint16_t* dscore;       // bf16 [capacity, C]   (backward)
   float* partial;         // fp32 [R, r, C]       (backward)
+  int32_t* status;        // backward: the call's status word in the workspace (see below)
   int32_t* dev_error;
+  long long wait_cycles;  // bound of each pipeline mbarrier wait, in SM clock cycles
+  int withhold_row;       // test hook: the producer of CTA (0, 0) never issues the copies of
+                          // this row of its range (-1: off), so that its waits run out
   int64_t capacity;
   int64_t out_rows;
   int S, r, coff, d, C, W;
@@ -73,6 +77,15 @@ struct PoolParams {
   int bar_off;      //   the full/empty mbarriers
   int box_rows;     // long windows: tokens per tensor box
 };
+
+// Backward: CTA (0, 0) records in the workspace's status word whether the call's
+// cu_seqlens and out_rows were valid (0) or not (1). The dAPE reduction reads it after
+// the pooling grid has completed and leaves dAPE untouched unless it is 0, so a rejected
+// call writes no output at all. Every CTA computes the same TC, so one writer suffices.
+__device__ __forceinline__ void publish_status(const PoolParams& p, int TC) {
+  if (p.status != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    *p.status = TC < 0 ? 1 : 0;
+}
 
 // Zeroes rows [row0, row0+nrows) of dKV and dScore over this CTA's column slice (both
 // halves at coff=2). Cooperative over the whole CTA.
@@ -110,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 2) pool_kernel(const PoolParams p) {
 
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums);
+  publish_status(p, TC);
   if (TC < 0) return;
   pdl_trigger();  // the next kernel (the dAPE reduction, or the caller's) may launch
 

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kGenericThreads) pool_generic_kernel(const Poo
 
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
+  publish_status(p, TC);
   if (TC < 0) return;
   pdl_trigger();  // the next kernel (the dAPE reduction, or the caller's) may launch
 

@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   }
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
+  publish_status(p, TC);
   if (TC < 0) return;
   pdl_trigger();  // the next kernel (the dAPE reduction, or the caller's) may launch
 
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         uint32_t ph = 0;          // (j / depth) & 1
         for (int j = 0; j < nrows;
              ++j, pslot = slot, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
-          if (!mbar_wait_bounded(&done[slot], ph) ||
+          if (!mbar_wait_bounded(&done[slot], ph, p.wait_cycles) ||
               *reinterpret_cast<volatile int*>(&s_abort)) {
             bad = true;
             break;
@@ -194,18 +195,20 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     // ------------------------------ producer ------------------------------------------
     if (tid == NCT) {
       const uint64_t pol = l2_evict_first_policy();
+      const int withheld = (blockIdx.x == 0 && blockIdx.y == 0) ? p.withhold_row : -1;
       int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
       int j = 0;
       int slot = 0;     // j % depth
       uint32_t ph = 0;  // (j / depth) & 1
       for (; j < nrows; ++j, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
-        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u)) {
+        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u, p.wait_cycles)) {
           s_abort = 1;
           break;
         }
         if (*reinterpret_cast<volatile int*>(&s_abort)) break;
         const int o = o0 + j;
         s = advance_segment(sB, s, o);
+        if (j == withheld) continue;  // test hook: this stage never fills
         const int b = o - sB[s];
         const int base = sCu[s] + b * r;
         const bool has_prev = two && b >= 1;
@@ -227,11 +230,14 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
                          p.dout + static_cast<int64_t>(o) * d + col0, kLongSlice * 2,
                          &full[slot], pol);
       }
-      if (j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) {
-        if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
-        for (int k = max(0, j - p.depth); k < j; ++k)
-          mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1));
-      }
+      if ((j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) && p.dev_error != nullptr)
+        *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;  // stopped early
+      // Every copy issued here lands before the CTA can exit (consumers that stop early
+      // do not wait for them; slots of rows before j - depth were handed back, so landed).
+      for (int k = max(0, j - p.depth); k < j; ++k)
+        if (k != withheld)
+          mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1),
+                            kWaitCycles);
     }
     return;
   }
@@ -299,11 +305,13 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     const int b = o - sB[s];
     const int base = sCu[s] + b * r;
     const bool has_prev = two && b >= 1;
-    const bool ok = mbar_wait_bounded(&full[slot], ph);
-    if (!__all_sync(0xFFFFFFFFu, ok) || *reinterpret_cast<volatile int*>(&s_abort)) {
+    const bool ok = mbar_wait_bounded(&full[slot], ph, p.wait_cycles);
+    if (!__all_sync(0xFFFFFFFFu, ok)) {  // a copy wait ran out: stop, and say so
       s_abort = 1;
+      if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
       break;
     }
+    if (__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s_abort) != 0)) break;
     unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
 
     // x' = score*log2e + ape' at this thread's slots; invalid (first block, previous half)

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
   // (the block prefix ends with a barrier: the mbarriers are ready after it)
   const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
+  publish_status(p, TC);
   if (TC < 0) return;
   pdl_trigger();  // the next kernel (the dAPE reduction, or the caller's) may launch
 
@@ -144,17 +145,19 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
       if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, V, lane - 32, 32);
     }
     if (lane == 0) {
+      const int withheld = (blockIdx.x == 0 && blockIdx.y == 0) ? p.withhold_row : -1;
       int j = 0;
       int slot = 0;       // j % depth
       uint32_t ph = 0;    // (j / depth) & 1
       for (; j < nrows; ++j, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
-        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u)) {
+        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u, p.wait_cycles)) {
           s_abort = 1;
           break;
         }
         if (*reinterpret_cast<volatile int*>(&s_abort)) break;
         const int o = o0 + j;
         s = advance_segment(sB, s, o);
+        if (j == withheld) continue;  // test hook: this stage never fills
         const int base = sCu[s] + (o - sB[s]) * R;
         unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
         mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_g + (BWD ? d * 2 : 0)));
@@ -164,13 +167,16 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
         if constexpr (BWD)
           bulk_load_hint(st + stage_g, p.dout + static_cast<int64_t>(o) * d, d * 2, &full[slot], pol);
       }
-      if (j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) {
-        // stopping early: let every issued copy land before the CTA can exit
-        if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
-        for (int k = max(0, j - p.depth); k < j; ++k)
-          mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1));
-        if (need_pre) mbar_wait_bounded(pre_bar, 0);
-      }
+      if ((j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) && p.dev_error != nullptr)
+        *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;  // stopped early
+      // Every copy issued here lands before the CTA can exit: normally the consumers have
+      // waited for all of them already, but consumers that stop early have not. (Slots of
+      // rows before j - depth were handed back by the consumers, so their copies landed.)
+      for (int k = max(0, j - p.depth); k < j; ++k)
+        if (k != withheld)
+          mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1),
+                            kWaitCycles);
+      if (need_pre) mbar_wait_bounded(pre_bar, 0, kWaitCycles);
     }
   } else {
     // ------------------------------ consumers -----------------------------------------
@@ -211,7 +217,7 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
         const int cs = sCu[s];
         const int base = cs + b * R;
         const bool has_prev = TWO && b >= 1;
-        bool ok = mbar_wait_bounded(&full[slot], ph);
+        bool ok = mbar_wait_bounded(&full[slot], ph, p.wait_cycles);
         // kv chunk of the own block's first token; score sits kv_bytes further, rows are C2
         // bytes apart. The previous block (coff=2) uses the same layout (its own stage, or
         // the block fetched before the first row).
@@ -221,17 +227,19 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
         const unsigned char* prev_kv = nullptr;
         if (has_prev) {
           if (j == 0) {
-            ok = ok && mbar_wait_bounded(pre_bar, 0);
+            ok = ok && mbar_wait_bounded(pre_bar, 0, p.wait_cycles);
             prev_kv = pre + c0 * 2;
           } else {
-            ok = ok && mbar_wait_bounded(&full[pslot], pph);
+            ok = ok && mbar_wait_bounded(&full[pslot], pph, p.wait_cycles);
             prev_kv = stages + static_cast<size_t>(pslot) * p.stage_bytes + c0 * 2;
           }
         }
-        if (!ok || *reinterpret_cast<volatile int*>(&s_abort)) {
+        if (!ok) {  // a copy wait ran out: stop, and say so
           s_abort = 1;
+          if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
           break;
         }
+        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
 
         // x' = score*log2e + ape*log2e for window position i (column pairs)
         uint64_t x[W][NW];

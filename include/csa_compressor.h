@@ -57,16 +57,18 @@ typedef struct CUstream_st* csa_stream_t;
 
 typedef enum {
   CSA_OK = 0,
-  CSA_ERR_INVALID_VALUE = 1, /* NULL pointer, negative size, misaligned pointer, small workspace */
+  CSA_ERR_INVALID_VALUE = 1, /* NULL pointer, negative size, misaligned pointer */
   CSA_ERR_UNSUPPORTED = 2,   /* coff not in {1,2}, size limits below */
-  CSA_ERR_CUDA = 3           /* a CUDA runtime call or kernel launch failed */
+  CSA_ERR_WORKSPACE = 3,     /* backward workspace NULL or smaller than the query's size */
+  CSA_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
 } csa_status_t;
 
 /* Codes the kernels write to *dev_error. */
 #define CSA_DEVERR_CU_SEQLENS 1 /* cu_seqlens[0] < 0, decreasing, or cu_seqlens[S] > capacity */
 #define CSA_DEVERR_OUT_ROWS 2   /* total_comp > out_rows */
 #define CSA_DEVERR_TIMEOUT 3    /* a wait for an asynchronous copy gave up (about 2 s); the
-                                   kernel stopped early, outputs are incomplete */
+                                   kernel stopped early, outputs (dAPE included) are
+                                   incomplete */
 
 /* Limits checked on the host (CSA_ERR_UNSUPPORTED beyond them). */
 #define CSA_MAX_SEGMENTS 16384   /* S */
@@ -102,7 +104,9 @@ csa_status_t csa_compressor_fwd(const void* kv, const void* score, const float* 
                                 int64_t out_rows, int32_t* dev_error, csa_stream_t stream);
 
 /* Bytes of device workspace csa_compressor_bwd needs for these sizes on the current
- * device (per-row-group dAPE partial sums; reduced in a fixed order). 0 on bad sizes. */
+ * device: per-row-group dAPE partial sums (reduced in a fixed order) and a 16-byte status
+ * block through which the pooling kernel tells the reduction whether the call's
+ * cu_seqlens were valid. 0 on bad sizes. */
 size_t csa_compressor_bwd_workspace_bytes(int32_t S, int32_t ratio, int32_t coff, int32_t d,
                                           int64_t capacity, int64_t out_rows);
 
@@ -112,9 +116,11 @@ size_t csa_compressor_bwd_workspace_bytes(int32_t S, int32_t ratio, int32_t coff
  *   dout        bf16 [out_rows, d] (device); rows >= total_comp are not read
  *   dkv, dscore bf16 [capacity, coff*d] (device): EVERY element is written
  *   dape        fp32 [ratio, coff*d] (device): accumulate_dape = 0 stores the sum,
- *               1 adds it to the current contents
+ *               1 adds it to the current contents; left untouched when the device
+ *               rejects cu_seqlens or out_rows
  *   workspace   device scratch of at least csa_compressor_bwd_workspace_bytes(...)
- *               bytes, 16-byte aligned; contents on entry do not matter
+ *               bytes (CSA_ERR_WORKSPACE otherwise), 16-byte aligned for the vector
+ *               kernels; contents on entry do not matter
  * Two kernels are enqueued: the pooling backward and a fixed-order dAPE reduction. */
 csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* ape,
                                 const int32_t* cu_seqlens, const void* dout, int32_t S,
@@ -146,6 +152,23 @@ csa_status_t csa_compressor_bwd_noalloc(const void* kv, const void* score, const
                                         int64_t out_rows, void* dkv, void* dscore, float* dape,
                                         int32_t accumulate_dape, int32_t* dev_error,
                                         csa_stream_t stream);
+
+/* Smallest non-zero wait bound csa_compressor_test_hooks accepts, in SM clock cycles. */
+#define CSA_TEST_MIN_WAIT_CYCLES 1000000
+
+/* Test hook for the bounded waits: lets a test make a pipeline wait run out without any
+ * fault. The pages have no counterpart; it is this library's own.
+ *   wait_cycles   bound of every later pooling launch's pipeline waits, in SM clock
+ *                 cycles (CSA_TEST_MIN_WAIT_CYCLES .. about 2 s); 0 restores the default
+ *                 of about 2 s
+ *   withhold_row  >= 0: in every later launch of a bulk-copy kernel (the block-streaming
+ *                 and long-window kernels), the producer of CTA (0, 0) skips the copies
+ *                 of row `withhold_row` of its row range, so the waits for that stage run
+ *                 out, the kernel writes CSA_DEVERR_TIMEOUT to *dev_error, lets its own
+ *                 copies land and returns; < 0: off (the default)
+ * Process-wide; applies to calls made after it returns, from any host thread.
+ * CSA_ERR_INVALID_VALUE for a bound outside the range above. */
+csa_status_t csa_compressor_test_hooks(int64_t wait_cycles, int32_t withhold_row);
 
 /* Index map only (the THD segment/block mapping the pooling kernels use), for
  * checking it bit for bit: for every output row o < out_rows writes

@@ -29,7 +29,7 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
         return out
     cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-shared",
-           "-fPIC", "-o", out, src]
+           "-fPIC", "-pthread", "-o", out, src]
     subprocess.run(cmd, check=True)
     return out
 
@@ -57,6 +57,13 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_oracle_bwd.restype = i32
     lib.csa_oracle_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i64,
                                    vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.csa_oracle_fwd_threads.restype = i32
+    lib.csa_oracle_fwd_threads.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64, i64, vp, i32]
+    lib.csa_oracle_bwd_threads.restype = i32
+    lib.csa_oracle_bwd_threads.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i64,
+                                           vp, vp, vp, i32]
+    lib.csa_oracle_hardware_threads.restype = i32
+    lib.csa_oracle_hardware_threads.argtypes = []
     lib.csa_oracle_round_bf16.restype = None
     lib.csa_oracle_round_bf16.argtypes = [vp, i64, vp]
     if path is None:
@@ -150,6 +157,41 @@ def bwd(kv, score, ape, cu_seqlens, dout, ratio: int, coff: int, d: int, capacit
                               _p(res.get("dscore_f64")), _p(res["dape_f32"]),
                               _p(res.get("owners")), _p(res.get("dscore_err")),
                               _p(res.get("dape_err")), _p(res.get("dape_abs"))), "bwd")
+    return res
+
+
+def hardware_threads(lib: Optional[ctypes.CDLL] = None) -> int:
+    """Host threads the machine offers (std::thread::hardware_concurrency)."""
+    return int((lib or load()).csa_oracle_hardware_threads())
+
+
+def fwd_threads(pack, nthreads: int, lib: Optional[ctypes.CDLL] = None) -> np.ndarray:
+    """Forward on ``nthreads`` host threads (output-row ranges); returns out bits."""
+    lib = lib or load()
+    cu = _c(pack.cu_seqlens, np.int32)
+    kv, score, ape = _c(pack.kv, np.uint16), _c(pack.score, np.uint16), _c(pack.ape, np.float32)
+    out = np.zeros((pack.total_comp, pack.d), dtype=np.uint16)
+    _check(lib.csa_oracle_fwd_threads(_p(kv), _p(score), _p(ape), _p(cu), cu.shape[0] - 1,
+                                      pack.ratio, pack.coff, pack.d, pack.capacity,
+                                      pack.total_comp, _p(out), nthreads), "fwd_threads")
+    return out
+
+
+def bwd_threads(pack, nthreads: int, lib: Optional[ctypes.CDLL] = None) -> Dict[str, np.ndarray]:
+    """Backward on ``nthreads`` host threads; returns dkv, dscore bits and dape_f64."""
+    lib = lib or load()
+    cu = _c(pack.cu_seqlens, np.int32)
+    kv, score, ape = _c(pack.kv, np.uint16), _c(pack.score, np.uint16), _c(pack.ape, np.float32)
+    dout = _c(pack.dout, np.uint16)
+    C = pack.coff * pack.d
+    res = {"dkv": np.empty((pack.capacity, C), dtype=np.uint16),
+           "dscore": np.empty((pack.capacity, C), dtype=np.uint16),
+           "dape_f64": np.empty((pack.ratio, C), dtype=np.float64)}
+    _check(lib.csa_oracle_bwd_threads(_p(kv), _p(score), _p(ape), _p(cu), _p(dout),
+                                      cu.shape[0] - 1, pack.ratio, pack.coff, pack.d,
+                                      pack.capacity, pack.total_comp, _p(res["dkv"]),
+                                      _p(res["dscore"]), _p(res["dape_f64"]), nthreads),
+           "bwd_threads")
     return res
 
 

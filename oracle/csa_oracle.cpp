@@ -45,6 +45,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <thread>
 #include <vector>
 
 namespace {
@@ -96,6 +97,36 @@ int64_t count_blocks(const int32_t* cu, int S, int ratio) {
   int64_t total = 0;
   for (int s = 0; s < S; ++s) total += (cu[s + 1] - cu[s]) / ratio;
   return total;
+}
+
+// The output rows in order: row o is block `b` of the segment starting at token `c`.
+struct BlockRef {
+  int64_t c;
+  int64_t b;
+};
+
+std::vector<BlockRef> list_blocks(const int32_t* cu, int S, int ratio) {
+  std::vector<BlockRef> rows;
+  for (int s = 0; s < S; ++s) {
+    const int64_t n = (cu[s + 1] - cu[s]) / ratio;
+    for (int64_t b = 0; b < n; ++b) rows.push_back({cu[s], b});
+  }
+  return rows;
+}
+
+// Runs fn(t, begin, end) for t = 0..nthreads-1 over contiguous, nearly equal ranges of
+// [0, rows) (output rows, or slots), on nthreads threads (the calling thread when
+// nthreads is 1).
+template <typename Fn>
+void over_row_ranges(int64_t rows, int nthreads, Fn fn) {
+  if (nthreads <= 1) {
+    fn(0, int64_t{0}, rows);
+    return;
+  }
+  std::vector<std::thread> pool;
+  for (int t = 0; t < nthreads; ++t)
+    pool.emplace_back(fn, t, rows * t / nthreads, rows * (t + 1) / nthreads);
+  for (std::thread& th : pool) th.join();
 }
 
 // One valid position of a pooling window: the token row and column it reads in
@@ -181,6 +212,135 @@ double output_error_mass(const WindowStats& st) {
   return a;
 }
 
+// Forward over nthreads threads, each taking a contiguous range of output rows (the
+// per-element arithmetic is the same whatever the thread count).
+int fwd_impl(const uint16_t* kv, const uint16_t* score, const float* ape,
+             const int32_t* cu_seqlens, int S, int ratio, int coff, int d, int64_t capacity,
+             int64_t out_rows, uint16_t* out_bf16, double* out_f64, double* out_err,
+             int nthreads) {
+  int rc = check_args(cu_seqlens, S, ratio, coff, d, capacity);
+  if (rc != ORACLE_OK) return rc;
+  if (kv == nullptr || score == nullptr || ape == nullptr || out_bf16 == nullptr)
+    return ORACLE_BAD_ARGS;
+  if (count_blocks(cu_seqlens, S, ratio) > out_rows) return ORACLE_OUT_ROWS;
+  const int64_t C = static_cast<int64_t>(coff) * d;
+  const std::vector<BlockRef> rows = list_blocks(cu_seqlens, S, ratio);
+  over_row_ranges(static_cast<int64_t>(rows.size()), nthreads,
+                  [&](int, int64_t o_begin, int64_t o_end) {
+    std::vector<WindowPos> win;
+    WindowStats st;
+    for (int64_t o = o_begin; o < o_end; ++o) {
+      for (int64_t j = 0; j < d; ++j) {
+        window_of(rows[o].c, rows[o].b, ratio, coff, d, j, win);
+        window_stats(kv, score, ape, C, win, st);
+        out_bf16[o * d + j] = double_to_bf16_bits(st.o);
+        if (out_f64 != nullptr) out_f64[o * d + j] = st.o;
+        if (out_err != nullptr) out_err[o * d + j] = output_error_mass(st);
+      }
+    }
+  });
+  return ORACLE_OK;
+}
+
+// Backward over nthreads threads (contiguous output-row ranges). Every slot is read by
+// at most one window position, so the threads write disjoint slots; each thread sums its
+// rows' dAPE terms, and the thread sums are added in thread order at the end (with one
+// thread: the plain sum over rows in order).
+int bwd_impl(const uint16_t* kv, const uint16_t* score, const float* ape,
+             const int32_t* cu_seqlens, const uint16_t* dout, int S, int ratio, int coff, int d,
+             int64_t capacity, int64_t out_rows, uint16_t* dkv_bf16, uint16_t* dscore_bf16,
+             double* dape_f64, double* dkv_f64, double* dscore_f64, float* dape_f32,
+             int32_t* owners, double* dscore_err, double* dape_err, double* dape_abs,
+             int nthreads) {
+  int rc = check_args(cu_seqlens, S, ratio, coff, d, capacity);
+  if (rc != ORACLE_OK) return rc;
+  if (kv == nullptr || score == nullptr || ape == nullptr || dkv_bf16 == nullptr ||
+      dscore_bf16 == nullptr || dape_f64 == nullptr)
+    return ORACLE_BAD_ARGS;
+  const int64_t total = count_blocks(cu_seqlens, S, ratio);
+  if (total > out_rows) return ORACLE_OUT_ROWS;
+  if (total > 0 && dout == nullptr) return ORACLE_BAD_ARGS;
+  const int64_t C = static_cast<int64_t>(coff) * d;
+  const int64_t slots = capacity * C;
+  const int64_t napes = static_cast<int64_t>(ratio) * C;
+  if (nthreads < 1) nthreads = 1;
+
+  // Every slot starts as an exact +0; consumed slots are overwritten below.
+  std::vector<double> gkv(static_cast<size_t>(slots), 0.0);
+  std::vector<double> gsc(static_cast<size_t>(slots), 0.0);
+  std::vector<double> gsc_err(dscore_err != nullptr ? static_cast<size_t>(slots) : 0, 0.0);
+  std::vector<int32_t> count(static_cast<size_t>(slots), 0);
+  // per-thread dAPE sums: value, error mass, absolute terms
+  std::vector<std::vector<double>> t_dape(nthreads, std::vector<double>(napes, 0.0));
+  std::vector<std::vector<double>> t_err(nthreads, std::vector<double>(napes, 0.0));
+  std::vector<std::vector<double>> t_abs(nthreads, std::vector<double>(napes, 0.0));
+
+  const std::vector<BlockRef> rows = list_blocks(cu_seqlens, S, ratio);
+  over_row_ranges(static_cast<int64_t>(rows.size()), nthreads,
+                  [&](int t, int64_t o_begin, int64_t o_end) {
+    std::vector<WindowPos> win;
+    WindowStats st;
+    std::vector<double>& my_dape = t_dape[t];
+    std::vector<double>& my_err = t_err[t];
+    std::vector<double>& my_abs = t_abs[t];
+    for (int64_t o = o_begin; o < o_end; ++o) {
+      for (int64_t j = 0; j < d; ++j) {
+        window_of(rows[o].c, rows[o].b, ratio, coff, d, j, win);
+        window_stats(kv, score, ape, C, win, st);
+        const double g = bf16_bits_to_double(dout[o * d + j]);
+        const double oerr = output_error_mass(st);
+        for (size_t i = 0; i < win.size(); ++i) {
+          const int64_t flat = win[i].token * C + win[i].col;
+          // d out / d kv_w = p_w ; d out / d x_w = p_w (kv_w - out)  (softmax Jacobian)
+          const double dk = st.p[i] * g;
+          const double ds = st.p[i] * g * (st.v[i] - st.o);
+          gkv[flat] = dk;
+          gsc[flat] = ds;
+          count[flat] += 1;
+          my_dape[win[i].ape_index] += ds;
+          const double err = std::fabs(st.p[i] * g) *
+                             (std::fabs(st.v[i] - st.o) *
+                                  (1.0 + std::fabs(st.x[i]) + std::fabs(st.m)) +
+                              oerr);
+          if (dscore_err != nullptr) gsc_err[flat] = err;
+          my_err[win[i].ape_index] += err + std::fabs(ds);
+          my_abs[win[i].ape_index] += std::fabs(ds);
+        }
+      }
+    }
+  });
+
+  for (int64_t i = 0; i < napes; ++i) {
+    double v = 0.0, e = 0.0, a = 0.0;
+    for (int t = 0; t < nthreads; ++t) {
+      v += t_dape[t][i];
+      e += t_err[t][i];
+      a += t_abs[t][i];
+    }
+    dape_f64[i] = v;
+    if (dape_err != nullptr) dape_err[i] = e;
+    if (dape_abs != nullptr) dape_abs[i] = a;
+  }
+  // every slot rounded (and its owner count checked), over slot ranges per thread
+  std::vector<int> twice(nthreads, 0);
+  over_row_ranges(slots, nthreads, [&](int t, int64_t i0, int64_t i1) {
+    for (int64_t i = i0; i < i1; ++i) {
+      if (count[i] > 1) twice[t] = 1;
+      dkv_bf16[i] = double_to_bf16_bits(gkv[i]);
+      dscore_bf16[i] = double_to_bf16_bits(gsc[i]);
+      if (dkv_f64 != nullptr) dkv_f64[i] = gkv[i];
+      if (dscore_f64 != nullptr) dscore_f64[i] = gsc[i];
+      if (owners != nullptr) owners[i] = count[i];
+      if (dscore_err != nullptr) dscore_err[i] = gsc_err[i];
+    }
+  });
+  for (int t = 0; t < nthreads; ++t)
+    if (twice[t]) return ORACLE_DOUBLE_WRITE;
+  if (dape_f32 != nullptr)
+    for (int64_t i = 0; i < napes; ++i) dape_f32[i] = static_cast<float>(dape_f64[i]);
+  return ORACLE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -222,29 +382,8 @@ int csa_oracle_fwd(const uint16_t* kv, const uint16_t* score, const float* ape,
                    const int32_t* cu_seqlens, int S, int ratio, int coff, int d,
                    int64_t capacity, int64_t out_rows, uint16_t* out_bf16, double* out_f64,
                    double* out_err) {
-  int rc = check_args(cu_seqlens, S, ratio, coff, d, capacity);
-  if (rc != ORACLE_OK) return rc;
-  if (kv == nullptr || score == nullptr || ape == nullptr || out_bf16 == nullptr)
-    return ORACLE_BAD_ARGS;
-  if (count_blocks(cu_seqlens, S, ratio) > out_rows) return ORACLE_OUT_ROWS;
-  const int64_t C = static_cast<int64_t>(coff) * d;
-  std::vector<WindowPos> win;
-  WindowStats st;
-  int64_t o = 0;
-  for (int s = 0; s < S; ++s) {
-    const int64_t c = cu_seqlens[s];
-    const int64_t n = (cu_seqlens[s + 1] - cu_seqlens[s]) / ratio;
-    for (int64_t b = 0; b < n; ++b, ++o) {
-      for (int64_t j = 0; j < d; ++j) {
-        window_of(c, b, ratio, coff, d, j, win);
-        window_stats(kv, score, ape, C, win, st);
-        out_bf16[o * d + j] = double_to_bf16_bits(st.o);
-        if (out_f64 != nullptr) out_f64[o * d + j] = st.o;
-        if (out_err != nullptr) out_err[o * d + j] = output_error_mass(st);
-      }
-    }
-  }
-  return ORACLE_OK;
+  return fwd_impl(kv, score, ape, cu_seqlens, S, ratio, coff, d, capacity, out_rows, out_bf16,
+                  out_f64, out_err, 1);
 }
 
 // Backward. dout: bf16 bits [out_rows, d]. Writes every element of dkv_bf16 and
@@ -260,74 +399,39 @@ int csa_oracle_bwd(const uint16_t* kv, const uint16_t* score, const float* ape,
                    uint16_t* dscore_bf16, double* dape_f64, double* dkv_f64, double* dscore_f64,
                    float* dape_f32, int32_t* owners, double* dscore_err, double* dape_err,
                    double* dape_abs) {
-  int rc = check_args(cu_seqlens, S, ratio, coff, d, capacity);
-  if (rc != ORACLE_OK) return rc;
-  if (kv == nullptr || score == nullptr || ape == nullptr || dkv_bf16 == nullptr ||
-      dscore_bf16 == nullptr || dape_f64 == nullptr)
-    return ORACLE_BAD_ARGS;
-  const int64_t total = count_blocks(cu_seqlens, S, ratio);
-  if (total > out_rows) return ORACLE_OUT_ROWS;
-  if (total > 0 && dout == nullptr) return ORACLE_BAD_ARGS;
-  const int64_t C = static_cast<int64_t>(coff) * d;
-  const int64_t slots = capacity * C;
+  return bwd_impl(kv, score, ape, cu_seqlens, dout, S, ratio, coff, d, capacity, out_rows,
+                  dkv_bf16, dscore_bf16, dape_f64, dkv_f64, dscore_f64, dape_f32, owners,
+                  dscore_err, dape_err, dape_abs, 1);
+}
 
-  // Every slot starts as an exact +0; consumed slots are overwritten below.
-  std::vector<double> gkv(static_cast<size_t>(slots), 0.0);
-  std::vector<double> gsc(static_cast<size_t>(slots), 0.0);
-  std::vector<double> gsc_err(dscore_err != nullptr ? static_cast<size_t>(slots) : 0, 0.0);
-  std::vector<int32_t> count(static_cast<size_t>(slots), 0);
-  for (int64_t i = 0; i < static_cast<int64_t>(ratio) * C; ++i) {
-    dape_f64[i] = 0.0;
-    if (dape_err != nullptr) dape_err[i] = 0.0;
-    if (dape_abs != nullptr) dape_abs[i] = 0.0;
-  }
+// The forward and backward on nthreads host threads (contiguous output-row ranges per
+// thread), for timing the oracle on all host cores. Same results as the single-thread
+// entry points (dAPE up to the order of its final additions). Returns ORACLE_BAD_ARGS
+// for nthreads < 1.
+int csa_oracle_fwd_threads(const uint16_t* kv, const uint16_t* score, const float* ape,
+                           const int32_t* cu_seqlens, int S, int ratio, int coff, int d,
+                           int64_t capacity, int64_t out_rows, uint16_t* out_bf16,
+                           int nthreads) {
+  if (nthreads < 1) return ORACLE_BAD_ARGS;
+  return fwd_impl(kv, score, ape, cu_seqlens, S, ratio, coff, d, capacity, out_rows, out_bf16,
+                  nullptr, nullptr, nthreads);
+}
 
-  std::vector<WindowPos> win;
-  WindowStats st;
-  int64_t o = 0;
-  for (int s = 0; s < S; ++s) {
-    const int64_t c = cu_seqlens[s];
-    const int64_t n = (cu_seqlens[s + 1] - cu_seqlens[s]) / ratio;
-    for (int64_t b = 0; b < n; ++b, ++o) {
-      for (int64_t j = 0; j < d; ++j) {
-        window_of(c, b, ratio, coff, d, j, win);
-        window_stats(kv, score, ape, C, win, st);
-        const double g = bf16_bits_to_double(dout[o * d + j]);
-        const double oerr = output_error_mass(st);
-        for (size_t i = 0; i < win.size(); ++i) {
-          const int64_t flat = win[i].token * C + win[i].col;
-          // d out / d kv_w = p_w ; d out / d x_w = p_w (kv_w - out)  (softmax Jacobian)
-          const double dk = st.p[i] * g;
-          const double ds = st.p[i] * g * (st.v[i] - st.o);
-          gkv[flat] = dk;
-          gsc[flat] = ds;
-          count[flat] += 1;
-          dape_f64[win[i].ape_index] += ds;
-          const double err = std::fabs(st.p[i] * g) *
-                             (std::fabs(st.v[i] - st.o) *
-                                  (1.0 + std::fabs(st.x[i]) + std::fabs(st.m)) +
-                              oerr);
-          if (dscore_err != nullptr) gsc_err[flat] = err;
-          if (dape_err != nullptr) dape_err[win[i].ape_index] += err + std::fabs(ds);
-          if (dape_abs != nullptr) dape_abs[win[i].ape_index] += std::fabs(ds);
-        }
-      }
-    }
-  }
+int csa_oracle_bwd_threads(const uint16_t* kv, const uint16_t* score, const float* ape,
+                           const int32_t* cu_seqlens, const uint16_t* dout, int S, int ratio,
+                           int coff, int d, int64_t capacity, int64_t out_rows,
+                           uint16_t* dkv_bf16, uint16_t* dscore_bf16, double* dape_f64,
+                           int nthreads) {
+  if (nthreads < 1) return ORACLE_BAD_ARGS;
+  return bwd_impl(kv, score, ape, cu_seqlens, dout, S, ratio, coff, d, capacity, out_rows,
+                  dkv_bf16, dscore_bf16, dape_f64, nullptr, nullptr, nullptr, nullptr, nullptr,
+                  nullptr, nullptr, nthreads);
+}
 
-  for (int64_t i = 0; i < slots; ++i) {
-    if (count[i] > 1) return ORACLE_DOUBLE_WRITE;
-    dkv_bf16[i] = double_to_bf16_bits(gkv[i]);
-    dscore_bf16[i] = double_to_bf16_bits(gsc[i]);
-    if (dkv_f64 != nullptr) dkv_f64[i] = gkv[i];
-    if (dscore_f64 != nullptr) dscore_f64[i] = gsc[i];
-    if (owners != nullptr) owners[i] = count[i];
-    if (dscore_err != nullptr) dscore_err[i] = gsc_err[i];
-  }
-  if (dape_f32 != nullptr)
-    for (int64_t i = 0; i < static_cast<int64_t>(ratio) * C; ++i)
-      dape_f32[i] = static_cast<float>(dape_f64[i]);
-  return ORACLE_OK;
+// Host threads the machine offers (std::thread::hardware_concurrency; at least 1).
+int csa_oracle_hardware_threads(void) {
+  const unsigned n = std::thread::hardware_concurrency();
+  return n == 0 ? 1 : static_cast<int>(n);
 }
 
 // Round doubles to bf16 bit patterns (exposed so the pins can test the rounding).

@@ -35,8 +35,22 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(4):
+    for code in range(5):
         assert gp.csa_status_string(code).startswith("CSA_")
+    assert gp.csa_status_string(gp.CSA_ERR_WORKSPACE).startswith("CSA_ERR_WORKSPACE")
+    assert gp.csa_status_string(gp.CSA_ERR_CUDA).startswith("CSA_ERR_CUDA")
+
+
+def test_status_codes_match_header():
+    text = open(HEADER).read()
+    for name in ("CSA_OK", "CSA_ERR_INVALID_VALUE", "CSA_ERR_UNSUPPORTED", "CSA_ERR_WORKSPACE",
+                 "CSA_ERR_CUDA"):
+        m = re.search(rf"\b{name} = (\d+)", text)
+        assert m and int(m.group(1)) == getattr(gp, name), name
+    for name in ("CSA_DEVERR_CU_SEQLENS", "CSA_DEVERR_OUT_ROWS", "CSA_DEVERR_TIMEOUT",
+                 "CSA_TEST_MIN_WAIT_CYCLES"):
+        m = re.search(rf"#define {name} (\d+)", text)
+        assert m and int(m.group(1)) == getattr(gp, name), name
 
 
 def test_total_comp_host_helper(lib, oracle_lib):
@@ -110,6 +124,10 @@ def test_fwd_rejects(lib, over, code):
     (dict(dape=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),
     (dict(ws=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),
     (dict(ratio=-2), gp.CSA_ERR_INVALID_VALUE),
+    # workspaces smaller than one row group's partials plus the status block
+    (dict(ws=None), gp.CSA_ERR_WORKSPACE),
+    (dict(ws_bytes=0), gp.CSA_ERR_WORKSPACE),
+    (dict(ws_bytes=4 * 16 * 4 + 15), gp.CSA_ERR_WORKSPACE),  # ratio 4 x C 16 fp32 + 16 - 1
 ])
 def test_bwd_rejects(lib, over, code):
     assert bwd_status(lib, **over) == code
@@ -118,6 +136,13 @@ def test_bwd_rejects(lib, over, code):
 def test_workspace_query_rejects_bad_sizes(lib):
     assert gp.csa_compressor_bwd_workspace_bytes(1, 4, 3, 8, 8, 2) == 0
     assert gp.csa_compressor_bwd_workspace_bytes(1, 200, 2, 12, 8, 2) == 0  # generic, window > 256
+
+
+def test_test_hooks_range(lib):
+    for bad in (-1, 1, gp.CSA_TEST_MIN_WAIT_CYCLES - 1, 5_000_000_000):
+        assert lib.csa_compressor_test_hooks(bad, -1) == gp.CSA_ERR_INVALID_VALUE
+    assert lib.csa_compressor_test_hooks(gp.CSA_TEST_MIN_WAIT_CYCLES, 3) == gp.CSA_OK
+    assert lib.csa_compressor_test_hooks(0, -1) == gp.CSA_OK  # back to the defaults
 
 
 def test_map_blocks_rejects(lib):

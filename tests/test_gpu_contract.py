@@ -100,6 +100,24 @@ def test_device_error_bad_cu_seqlens(cuda_lib):
     assert err == cuda_lib.CSA_DEVERR_CU_SEQLENS
 
 
+def test_rejected_call_leaves_dape_unchanged(cuda_lib):
+    """A backward whose cu_seqlens the device rejects writes no output at all: with
+    accumulate_dape=1 (and =0) the caller's dAPE keeps its bits, also after a valid call
+    has left its partials in the same workspace."""
+    import torch
+    pack = ts.make_pack("tiny")
+    dev = H.device_pack(pack)
+    H.run_bwd(cuda_lib, pack, dev=dev)  # a valid call first
+    bad = pack.cu_seqlens.copy()
+    bad[2] = bad[1] - 1
+    dev["cu_seqlens"] = torch.from_numpy(bad).cuda()
+    base = np.linspace(-1, 1, pack.ratio * pack.C, dtype=np.float32).reshape(pack.ratio, pack.C)
+    for acc in (1, 0):
+        _, _, dape, err = H.run_bwd(cuda_lib, pack, dev=dev, dape_init=base, accumulate=acc)
+        assert err == cuda_lib.CSA_DEVERR_CU_SEQLENS
+        assert (dape.view(np.uint32) == base.view(np.uint32)).all()
+
+
 def test_device_error_out_rows_too_small(cuda_lib):
     pack = ts.make_pack("tiny")
     out, err = H.run_fwd(cuda_lib, pack, out_rows=pack.total_comp - 1, prefill_bits=0x1234)
@@ -139,27 +157,46 @@ def test_non_default_stream(cuda_lib):
     assert e == 0 and (a == b).all()
 
 
+def _graph_packs():
+    """Two ragged ratio=2 coff=2 d=64 packs with the same segment count and token capacity
+    (static-capacity padding: 300 and 399 rows past cu_seqlens[S]), short and empty
+    segments, different lengths and values."""
+    a = ts.make_custom([700, 1, 3, 513, 0, 800], ratio=2, coff=2, d=64, pad_rows=300, seed=50)
+    b = ts.make_custom([300, 2, 900, 11, 5, 700], ratio=2, coff=2, d=64, pad_rows=399, seed=51)
+    assert a.capacity == b.capacity and a.S == b.S
+    return a, b
+
+
 def test_cuda_graph_capture_and_replay(cuda_lib):
-    """fwd + bwd captured once in a CUDA graph and replayed on new inputs copied into the
-    same buffers, with static-capacity padding rows (the graph case of the pages' zero
-    ownership): every replay matches an eager call on the same inputs, bit for bit."""
+    """fwd + bwd captured once in a CUDA graph and replayed on new inputs (other values
+    and other segment lengths) copied into the same buffers, with static-capacity padding
+    rows (the graph case of the pages' zero ownership, "Megatron-LM PR #5984", commits
+    "CSA: add fused Compressor..." and "fold dKV/dScore zero-init into the backward
+    kernel"): every replay, with its gradient buffers pre-filled with NaN, matches the
+    fp64 oracle on that replay's inputs under the parity tolerance."""
     import torch
-    a = ts.make_pack("ragged_r2_d512")
-    b = ts.make_pack("ragged_r2_d512", seed=5)
+    from tests.parity import compare_bf16, compare_dape
+    import oracle
+
+    a, b = _graph_packs()
+    S, r, coff, d, cap, C = a.S, a.ratio, a.coff, a.d, a.capacity, a.C
+    rows = max(a.total_comp, b.total_comp)  # out_rows: room for either pack's blocks
     dev = H.device_pack(a)
-    S, r, coff, d, cap, TC, C = a.S, a.ratio, a.coff, a.d, a.capacity, a.total_comp, a.C
-    out = torch.empty((TC, d), dtype=torch.bfloat16, device="cuda")
+    dev["dout"] = torch.zeros((rows, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((rows, d), dtype=torch.bfloat16, device="cuda")
     dkv = torch.empty((cap, C), dtype=torch.bfloat16, device="cuda")
     dsc = torch.empty_like(dkv)
     dape = torch.empty((r, C), dtype=torch.float32, device="cuda")
-    wsb = cuda_lib.csa_compressor_bwd_workspace_bytes(S, r, coff, d, cap, TC)
+    wsb = cuda_lib.csa_compressor_bwd_workspace_bytes(S, r, coff, d, cap, rows)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def step():
         cuda_lib.csa_compressor_fwd(dev["kv"], dev["score"], dev["ape"], dev["cu_seqlens"], S, r,
-                                    coff, d, cap, out, TC)
+                                    coff, d, cap, out, rows, err)
         cuda_lib.csa_compressor_bwd(dev["kv"], dev["score"], dev["ape"], dev["cu_seqlens"],
-                                    dev["dout"], S, r, coff, d, cap, TC, dkv, dsc, dape, 0, ws, wsb)
+                                    dev["dout"], S, r, coff, d, cap, rows, dkv, dsc, dape, 0, ws,
+                                    wsb, err)
 
     step()  # first call on this device sets up outside the capture
     torch.cuda.synchronize()
@@ -170,20 +207,35 @@ def test_cuda_graph_capture_and_replay(cuda_lib):
         with torch.cuda.graph(g, stream=side):
             step()
     torch.cuda.current_stream().wait_stream(side)
+    nan = np.int16(np.uint16(H.BF16_NAN).view(np.int16))
     for pack in (b, a, b):
         src = H.device_pack(pack)
-        for k in ("kv", "score", "ape", "dout"):
+        for k in ("kv", "score", "ape", "cu_seqlens"):
             dev[k].copy_(src[k])
-        dkv.view(torch.int16).fill_(np.int16(np.uint16(H.BF16_NAN).view(np.int16)))
-        dsc.copy_(dkv)
+        dev["dout"].zero_()
+        dev["dout"][:pack.total_comp].copy_(src["dout"])
+        dkv.view(torch.int16).fill_(nan)
+        dsc.view(torch.int16).fill_(nan)
+        dape.fill_(float("nan"))
+        err.zero_()
         g.replay()
         torch.cuda.synchronize()
-        got = (ts.bf16_tensor_bits(out), ts.bf16_tensor_bits(dkv), ts.bf16_tensor_bits(dsc),
-               dape.cpu().numpy())
-        ref_out, _ = H.run_fwd(cuda_lib, pack)
-        rk, rs, rd, _ = H.run_bwd(cuda_lib, pack)
-        assert (got[0] == ref_out).all() and (got[1] == rk).all() and (got[2] == rs).all()
-        assert (got[3].view(np.uint32) == rd.view(np.uint32)).all()
+        assert int(err.item()) == 0
+        TC = pack.total_comp
+        ref = oracle.fwd_pack(pack, want_f64=True, want_err=True)
+        refb = oracle.bwd_pack(pack, want_f64=True, want_err=True, want_owners=True)
+        got_out = ts.bf16_tensor_bits(out[:TC])
+        got_dkv, got_dsc = ts.bf16_tensor_bits(dkv), ts.bf16_tensor_bits(dsc)
+        reps = (compare_bf16("out", got_out, ref["out"], ref["out_f64"], ref["out_err"]),
+                compare_bf16("dkv", got_dkv, refb["dkv"], refb["dkv_f64"], np.abs(refb["dkv_f64"])),
+                compare_bf16("dscore", got_dsc, refb["dscore"], refb["dscore_f64"],
+                             refb["dscore_err"]),
+                compare_dape(dape.cpu().numpy(), refb["dape_f64"], refb["dape_err"]))
+        for rep in reps:
+            assert rep.fail == 0, str(rep)
+        zero = refb["owners"] == 0
+        assert (got_dkv.reshape(zero.shape)[zero] == 0).all()
+        assert (got_dsc.reshape(zero.shape)[zero] == 0).all()
 
 
 def test_back_to_back_calls_see_previous_results(cuda_lib):

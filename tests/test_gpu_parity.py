@@ -10,6 +10,9 @@ column slice, head dims that are not a multiple of 8 and pointers off 16-byte bo
 The tolerance is the one tests/parity.py derives; the count of elements that needed
 its cancellation clause is capped.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -21,6 +24,18 @@ from tests.parity import compare_bf16, compare_dape
 pytestmark = pytest.mark.gpu
 
 CLAUSE2_CAP = 2e-4  # fraction of elements allowed to need the cancellation clause
+
+
+def log_reports(label, *reports):
+    """Appends each report's counts to the JSON-lines file named by CSA_PARITY_LOG (if
+    set): how many elements were bit-exact and how many needed clause 2, per tensor."""
+    path = os.environ.get("CSA_PARITY_LOG")
+    if not path:
+        return
+    with open(path, "a") as fh:
+        for r in reports:
+            fh.write(json.dumps({"case": label, "tensor": r.name, "n": r.n, "exact": r.exact,
+                                 "clause2": r.clause2, "fail": r.fail}) + "\n")
 
 
 def small_packs():
@@ -101,18 +116,19 @@ SMALL = small_packs()
 FULL = ["tiny", "1x8192_d128", "3x8192_d512", "ragged_r2_d512", "long_r128_d512"]
 
 
-def check_fwd(gp, pack, shift=0):
+def check_fwd(gp, pack, shift=0, label=None):
     ref = oracle.fwd_pack(pack, want_f64=True, want_err=True)
     got, err = H.run_fwd(gp, pack, shift=shift)
     assert err == 0
     rep = compare_bf16("out", got, ref["out"], ref["out_f64"], ref["out_err"])
     print(pack.name, rep)
+    log_reports(label or pack.name, rep)
     assert rep.fail == 0, str(rep)
     assert rep.clause2 <= max(2, CLAUSE2_CAP * rep.n), str(rep)
     return rep
 
 
-def check_bwd(gp, pack, shift=0):
+def check_bwd(gp, pack, shift=0, label=None):
     ref = oracle.bwd_pack(pack, want_f64=True, want_err=True, want_owners=True)
     dkv, dsc, dape, err = H.run_bwd(gp, pack, shift=shift)
     assert err == 0
@@ -120,6 +136,7 @@ def check_bwd(gp, pack, shift=0):
     r2 = compare_bf16("dscore", dsc, ref["dscore"], ref["dscore_f64"], ref["dscore_err"])
     r3 = compare_dape(dape, ref["dape_f64"], ref["dape_err"])
     print(pack.name, r1, r2, r3, sep="\n  ")
+    log_reports(label or pack.name, r1, r2, r3)
     for rep in (r1, r2, r3):
         assert rep.fail == 0, str(rep)
     for rep in (r1, r2):
@@ -133,12 +150,12 @@ def check_bwd(gp, pack, shift=0):
 
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_fwd_small(cuda_lib, name):
-    check_fwd(cuda_lib, SMALL[name])
+    check_fwd(cuda_lib, SMALL[name], label=name)
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_bwd_small(cuda_lib, name):
-    check_bwd(cuda_lib, SMALL[name])
+    check_bwd(cuda_lib, SMALL[name], label=name)
 
 
 # pointers 2 (bf16) / 4 (fp32) bytes past a 16-byte boundary: the generic kernel, on shapes
@@ -148,12 +165,12 @@ MISALIGNED = ["tiny", "r4c2_d264", "r2c2_short_d64", "r16c1_d64", "r8c2_d128"]
 
 @pytest.mark.parametrize("name", MISALIGNED)
 def test_fwd_misaligned(cuda_lib, name):
-    check_fwd(cuda_lib, SMALL[name], shift=1)
+    check_fwd(cuda_lib, SMALL[name], shift=1, label=name + "+misaligned")
 
 
 @pytest.mark.parametrize("name", MISALIGNED)
 def test_bwd_misaligned(cuda_lib, name):
-    check_bwd(cuda_lib, SMALL[name], shift=1)
+    check_bwd(cuda_lib, SMALL[name], shift=1, label=name + "+misaligned")
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -43,3 +43,22 @@ def test_two_rank_aggregation():
 def test_single_rank_is_identity():
     assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]
     assert bench.whole_job_gbs(1, 2_000_000, 1.0) == pytest.approx(2.0)
+
+
+def test_replica_launch_end_to_end():
+    """The command bench.py runs for --gpus N without a torchrun environment starts N
+    ranks of one node on 127.0.0.1; run here with a CPU probe as the script, the ranks
+    rendezvous, aggregate over all of them, and rank 0 alone prints the line."""
+    import json
+    import subprocess
+    probe = os.path.join(os.path.dirname(os.path.abspath(__file__)), "replica_probe.py")
+    cmd = bench.replica_command(probe, ["--gpus", "2", "--steps", "3"], 2, bench.free_port())
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=180, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    out = json.loads(lines[0])
+    assert out["n_gpus"] == 2 and out["ms_per_step"] == 2.0
+    assert out["value"] == pytest.approx(2 * 1_000_000 / 2e-3 / 1e9)
+    assert out["argv"] == ["--gpus", "2", "--steps", "3"]

@@ -41,7 +41,7 @@ MUTANTS = {
     "softmax_not_normalised": ("for (size_t i = 0; i < n; ++i) st.p[i] /= z;", ""),
     "max_not_subtracted_and_first_only": (
         "st.p[i] = std::exp(st.x[i] - st.m);", "st.p[i] = std::exp(st.x[i] - st.x[0]) * (i == 0 ? 2.0 : 1.0);"),
-    "dape_sums_dkv": ("dape_f64[win[i].ape_index] += ds;", "dape_f64[win[i].ape_index] += dk;"),
+    "dape_sums_dkv": ("my_dape[win[i].ape_index] += ds;", "my_dape[win[i].ape_index] += dk;"),
     "score_grad_uses_kv_only": (
         "gsc[flat] = ds;", "gsc[flat] = dk;"),
 }

@@ -388,3 +388,20 @@ def test_oracle_rejects_bad_inputs(oracle_lib):
     with pytest.raises(oracle.OracleError):
         oracle.fwd(pack.kv, pack.score, pack.ape, pack.cu_seqlens, 4, 2, 8, pack.capacity,
                    out_rows=11)
+
+
+def test_threaded_oracle_matches_single_thread(oracle_lib):
+    """The multi-threaded drivers (used to time the oracle on every host core) give the
+    single-thread results: out, dKV, dScore bit for bit, dAPE up to the order of the final
+    additions of the per-thread sums."""
+    packs = [ts.make_custom([37, 12, 3, 0, 29], ratio=4, coff=2, d=8, pad_rows=5, seed=21),
+             ts.make_custom([9, 40, 1, 17], ratio=3, coff=1, d=5, pad_rows=2, seed=22)]
+    for pack in packs:
+        f1 = oracle.fwd_pack(pack)["out"]
+        b1 = oracle.bwd_pack(pack)
+        for nt in (1, 2, 3, 7):
+            assert (oracle.fwd_threads(pack, nt) == f1).all()
+            bt = oracle.bwd_threads(pack, nt)
+            assert (bt["dkv"] == b1["dkv"]).all() and (bt["dscore"] == b1["dscore"]).all()
+            np.testing.assert_allclose(bt["dape_f64"], b1["dape_f64"], rtol=1e-13, atol=1e-16)
+    assert oracle.hardware_threads() >= 1

@@ -18,17 +18,19 @@ from tests.parity import compare_bf16
 pytestmark = pytest.mark.gpu
 
 
-def _noalloc(gp, pack, dev):
+def _noalloc(gp, pack, dev, dape_init=None, accumulate=0):
     import torch
     C = pack.C
     fill = np.int16(np.uint16(H.BF16_NAN).view(np.int16))
     dkv = torch.full((pack.capacity, C), int(fill), dtype=torch.int16, device="cuda").view(torch.bfloat16)
     dsc = torch.full((pack.capacity, C), int(fill), dtype=torch.int16, device="cuda").view(torch.bfloat16)
     dape = torch.full((pack.ratio, C), float("nan"), dtype=torch.float32, device="cuda")
+    if dape_init is not None:
+        dape.copy_(torch.from_numpy(dape_init))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     gp.csa_compressor_bwd_noalloc(dev["kv"], dev["score"], dev["ape"], dev["cu_seqlens"],
                                   dev["dout"], pack.S, pack.ratio, pack.coff, pack.d,
-                                  pack.capacity, pack.total_comp, dkv, dsc, dape, 0, err)
+                                  pack.capacity, pack.total_comp, dkv, dsc, dape, accumulate, err)
     torch.cuda.synchronize()
     return ts.bf16_tensor_bits(dkv), ts.bf16_tensor_bits(dsc), dape.cpu().numpy(), int(err.item())
 
@@ -67,3 +69,21 @@ def test_noalloc_rejects_sizes_beyond_the_scratch(cuda_lib):
                                             dev["dout"], pack.S, pack.ratio, pack.coff, pack.d,
                                             pack.capacity, pack.total_comp, dkv, dsc, dape, 0)
     assert ei.value.status == cuda_lib.CSA_ERR_UNSUPPORTED
+
+
+def test_noalloc_rejected_call_leaves_dape_unchanged(cuda_lib):
+    """After a valid call has left its dAPE partials in the shared scratch array, a call
+    whose cu_seqlens the device rejects must not turn them into a dAPE: the caller's dAPE
+    keeps its bits, with accumulate_dape=1 and =0."""
+    import torch
+    pack = ts.make_pack("tiny")
+    dev = H.device_pack(pack)
+    assert _noalloc(cuda_lib, pack, dev)[3] == 0
+    bad = pack.cu_seqlens.copy()
+    bad[2] = bad[1] - 1
+    dev["cu_seqlens"] = torch.from_numpy(bad).cuda()
+    base = np.linspace(-1, 1, pack.ratio * pack.C, dtype=np.float32).reshape(pack.ratio, pack.C)
+    for acc in (1, 0):
+        _, _, dape, err = _noalloc(cuda_lib, pack, dev, dape_init=base, accumulate=acc)
+        assert err == cuda_lib.CSA_DEVERR_CU_SEQLENS
+        assert (dape.view(np.uint32) == base.view(np.uint32)).all()
