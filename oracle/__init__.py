@@ -56,7 +56,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_oracle_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64, i64, vp, vp, vp]
     lib.csa_oracle_bwd.restype = i32
     lib.csa_oracle_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i64,
-                                   vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                   vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.csa_oracle_fwd_threads.restype = i32
     lib.csa_oracle_fwd_threads.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64, i64, vp, i32]
     lib.csa_oracle_bwd_threads.restype = i32
@@ -128,7 +128,7 @@ def bwd(kv, score, ape, cu_seqlens, dout, ratio: int, coff: int, d: int, capacit
         want_err: bool = False, lib: Optional[ctypes.CDLL] = None) -> Dict[str, np.ndarray]:
     """Backward. Returns dkv/dscore (uint16 bf16 bits [capacity, coff*d]), dape_f64 and
     dape_f32 ([ratio, coff*d]); optionally the unrounded gradients, the per-slot owner
-    counts and the error masses."""
+    counts and the error masses (dkv_err, dscore_err, dape_err; dape_abs)."""
     lib = lib or load()
     cu = _c(cu_seqlens, np.int32)
     if out_rows is None:
@@ -148,6 +148,7 @@ def bwd(kv, score, ape, cu_seqlens, dout, ratio: int, coff: int, d: int, capacit
     if want_owners:
         res["owners"] = np.empty((capacity, C), dtype=np.int32)
     if want_err:
+        res["dkv_err"] = np.empty((capacity, C), dtype=np.float64)
         res["dscore_err"] = np.empty((capacity, C), dtype=np.float64)
         res["dape_err"] = np.empty((ratio, C), dtype=np.float64)
         res["dape_abs"] = np.empty((ratio, C), dtype=np.float64)
@@ -155,7 +156,8 @@ def bwd(kv, score, ape, cu_seqlens, dout, ratio: int, coff: int, d: int, capacit
                               ratio, coff, d, capacity, out_rows, _p(res["dkv"]),
                               _p(res["dscore"]), _p(res["dape_f64"]), _p(res.get("dkv_f64")),
                               _p(res.get("dscore_f64")), _p(res["dape_f32"]),
-                              _p(res.get("owners")), _p(res.get("dscore_err")),
+                              _p(res.get("owners")), _p(res.get("dkv_err")),
+                              _p(res.get("dscore_err")),
                               _p(res.get("dape_err")), _p(res.get("dape_abs"))), "bwd")
     return res
 

@@ -203,7 +203,11 @@ void window_stats(const uint16_t* kv, const uint16_t* score, const float* ape, i
 // can make in the output, in units of the fp32 unit roundoff: the summands'
 // magnitudes plus the spread of kv around the output weighted by how far each
 // weight's exponent argument is from zero (the absolute error of an fp32
-// exponent argument is proportional to |x| + |m|).
+// exponent argument is proportional to |x| + |m|). The weights' own errors enter
+// only through kv - out, since the normalisation makes them sum to one.
+// These masses are the tolerance machinery of the parity tests, not part of the
+// operation; tests/test_oracle_pins.py pins them to hand-derived closed forms and
+// to a plain float32 re-evaluation of every window.
 double output_error_mass(const WindowStats& st) {
   double a = 0.0;
   for (size_t i = 0; i < st.p.size(); ++i)
@@ -250,8 +254,8 @@ int bwd_impl(const uint16_t* kv, const uint16_t* score, const float* ape,
              const int32_t* cu_seqlens, const uint16_t* dout, int S, int ratio, int coff, int d,
              int64_t capacity, int64_t out_rows, uint16_t* dkv_bf16, uint16_t* dscore_bf16,
              double* dape_f64, double* dkv_f64, double* dscore_f64, float* dape_f32,
-             int32_t* owners, double* dscore_err, double* dape_err, double* dape_abs,
-             int nthreads) {
+             int32_t* owners, double* dkv_err, double* dscore_err, double* dape_err,
+             double* dape_abs, int nthreads) {
   int rc = check_args(cu_seqlens, S, ratio, coff, d, capacity);
   if (rc != ORACLE_OK) return rc;
   if (kv == nullptr || score == nullptr || ape == nullptr || dkv_bf16 == nullptr ||
@@ -269,6 +273,7 @@ int bwd_impl(const uint16_t* kv, const uint16_t* score, const float* ape,
   std::vector<double> gkv(static_cast<size_t>(slots), 0.0);
   std::vector<double> gsc(static_cast<size_t>(slots), 0.0);
   std::vector<double> gsc_err(dscore_err != nullptr ? static_cast<size_t>(slots) : 0, 0.0);
+  std::vector<double> gkv_err(dkv_err != nullptr ? static_cast<size_t>(slots) : 0, 0.0);
   std::vector<int32_t> count(static_cast<size_t>(slots), 0);
   // per-thread dAPE sums: value, error mass, absolute terms
   std::vector<std::vector<double>> t_dape(nthreads, std::vector<double>(napes, 0.0));
@@ -298,11 +303,13 @@ int bwd_impl(const uint16_t* kv, const uint16_t* score, const float* ape,
           gsc[flat] = ds;
           count[flat] += 1;
           my_dape[win[i].ape_index] += ds;
-          const double err = std::fabs(st.p[i] * g) *
-                             (std::fabs(st.v[i] - st.o) *
-                                  (1.0 + std::fabs(st.x[i]) + std::fabs(st.m)) +
-                              oerr);
+          // error masses (units of the fp32 unit roundoff): a weight p*g carries the
+          // error of its exponent argument, |x| + |m|, plus a rounding; dScore adds the
+          // error of kv - out, which is the output's
+          const double xm = 1.0 + std::fabs(st.x[i]) + std::fabs(st.m);
+          const double err = std::fabs(st.p[i] * g) * (std::fabs(st.v[i] - st.o) * xm + oerr);
           if (dscore_err != nullptr) gsc_err[flat] = err;
+          if (dkv_err != nullptr) gkv_err[flat] = std::fabs(dk) * xm;
           my_err[win[i].ape_index] += err + std::fabs(ds);
           my_abs[win[i].ape_index] += std::fabs(ds);
         }
@@ -332,6 +339,7 @@ int bwd_impl(const uint16_t* kv, const uint16_t* score, const float* ape,
       if (dscore_f64 != nullptr) dscore_f64[i] = gsc[i];
       if (owners != nullptr) owners[i] = count[i];
       if (dscore_err != nullptr) dscore_err[i] = gsc_err[i];
+      if (dkv_err != nullptr) dkv_err[i] = gkv_err[i];
     }
   });
   for (int t = 0; t < nthreads; ++t)
@@ -390,18 +398,18 @@ int csa_oracle_fwd(const uint16_t* kv, const uint16_t* score, const float* ape,
 // dscore_bf16 ([capacity, coff*d]) and dape_f64 ([ratio, coff*d], the sum over all
 // blocks, overwritten). Optional (may be NULL): dkv_f64/dscore_f64 (unrounded),
 // dape_f32 (dape rounded to fp32), owners (int32 [capacity, coff*d]: how many
-// window positions read the slot; must be 0 or 1), dscore_err and dape_err (first-
-// order fp32 error masses in units of the fp32 unit roundoff), dape_abs (sum of
-// the absolute values of the terms of each dAPE entry).
+// window positions read the slot; must be 0 or 1), dkv_err, dscore_err and dape_err
+// (first-order fp32 error masses in units of the fp32 unit roundoff), dape_abs (sum
+// of the absolute values of the terms of each dAPE entry).
 int csa_oracle_bwd(const uint16_t* kv, const uint16_t* score, const float* ape,
                    const int32_t* cu_seqlens, const uint16_t* dout, int S, int ratio, int coff,
                    int d, int64_t capacity, int64_t out_rows, uint16_t* dkv_bf16,
                    uint16_t* dscore_bf16, double* dape_f64, double* dkv_f64, double* dscore_f64,
-                   float* dape_f32, int32_t* owners, double* dscore_err, double* dape_err,
-                   double* dape_abs) {
+                   float* dape_f32, int32_t* owners, double* dkv_err, double* dscore_err,
+                   double* dape_err, double* dape_abs) {
   return bwd_impl(kv, score, ape, cu_seqlens, dout, S, ratio, coff, d, capacity, out_rows,
                   dkv_bf16, dscore_bf16, dape_f64, dkv_f64, dscore_f64, dape_f32, owners,
-                  dscore_err, dape_err, dape_abs, 1);
+                  dkv_err, dscore_err, dape_err, dape_abs, 1);
 }
 
 // The forward and backward on nthreads host threads (contiguous output-row ranges per
@@ -425,7 +433,7 @@ int csa_oracle_bwd_threads(const uint16_t* kv, const uint16_t* score, const floa
   if (nthreads < 1) return ORACLE_BAD_ARGS;
   return bwd_impl(kv, score, ape, cu_seqlens, dout, S, ratio, coff, d, capacity, out_rows,
                   dkv_bf16, dscore_bf16, dape_f64, nullptr, nullptr, nullptr, nullptr, nullptr,
-                  nullptr, nullptr, nthreads);
+                  nullptr, nullptr, nullptr, nthreads);
 }
 
 // Host threads the machine offers (std::thread::hardware_concurrency; at least 1).

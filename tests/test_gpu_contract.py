@@ -227,7 +227,7 @@ def test_cuda_graph_capture_and_replay(cuda_lib):
         got_out = ts.bf16_tensor_bits(out[:TC])
         got_dkv, got_dsc = ts.bf16_tensor_bits(dkv), ts.bf16_tensor_bits(dsc)
         reps = (compare_bf16("out", got_out, ref["out"], ref["out_f64"], ref["out_err"]),
-                compare_bf16("dkv", got_dkv, refb["dkv"], refb["dkv_f64"], np.abs(refb["dkv_f64"])),
+                compare_bf16("dkv", got_dkv, refb["dkv"], refb["dkv_f64"], refb["dkv_err"]),
                 compare_bf16("dscore", got_dsc, refb["dscore"], refb["dscore_f64"],
                              refb["dscore_err"]),
                 compare_dape(dape.cpu().numpy(), refb["dape_f64"], refb["dape_err"]))

@@ -132,7 +132,7 @@ def check_bwd(gp, pack, shift=0, label=None):
     ref = oracle.bwd_pack(pack, want_f64=True, want_err=True, want_owners=True)
     dkv, dsc, dape, err = H.run_bwd(gp, pack, shift=shift)
     assert err == 0
-    r1 = compare_bf16("dkv", dkv, ref["dkv"], ref["dkv_f64"], np.abs(ref["dkv_f64"]))
+    r1 = compare_bf16("dkv", dkv, ref["dkv"], ref["dkv_f64"], ref["dkv_err"])
     r2 = compare_bf16("dscore", dsc, ref["dscore"], ref["dscore_f64"], ref["dscore_err"])
     r3 = compare_dape(dape, ref["dape_f64"], ref["dape_err"])
     print(pack.name, r1, r2, r3, sep="\n  ")

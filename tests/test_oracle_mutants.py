@@ -1,10 +1,11 @@
 """Planted mistakes: each mutant of the oracle source must fail at least one pin.
 
 A mutant is a copy of oracle/csa_oracle.cpp with one plausible mistake (a swapped
-half, a reversed ape row, a dropped term, a flipped sign, an off-by-one mask),
+half, a reversed ape row, a dropped term, a flipped sign, an off-by-one mask, an error
+mass of the parity tolerance shrunk or inflated),
 compiled to a temporary library on the CPU. The pins re-run against it are the
-brute-force evaluator, the hand-derived golden pack and the softmax identities
-from test_oracle_pins.py. No mutant reads outside its buffers.
+brute-force evaluator, the hand-derived golden pack (values and error masses) and
+the softmax identities from test_oracle_pins.py. No mutant reads outside its buffers.
 """
 import json
 import math
@@ -17,7 +18,7 @@ import pytest
 
 import oracle
 import thd_synth as ts
-from tests.test_oracle_pins import GOLDEN, brute_force, tiny_packs
+from tests.test_oracle_pins import GOLDEN, brute_force, golden_mass_mismatches, tiny_packs
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "csa_oracle.cpp")
 
@@ -44,6 +45,17 @@ MUTANTS = {
     "dape_sums_dkv": ("my_dape[win[i].ape_index] += ds;", "my_dape[win[i].ape_index] += dk;"),
     "score_grad_uses_kv_only": (
         "gsc[flat] = ds;", "gsc[flat] = dk;"),
+    # the parity tolerance's error masses: each shrunk or inflated mass must fail a pin
+    "out_err_without_exponent_term": (
+        "std::fabs(st.v[i] - st.o) * (1.0 + std::fabs(st.x[i]) + std::fabs(st.m)));",
+        "std::fabs(st.v[i] - st.o));"),
+    "out_err_doubled": ("  return a;\n}", "  return 2.0 * a;\n}"),
+    "dkv_err_without_exponent_term": (
+        "gkv_err[flat] = std::fabs(dk) * xm;", "gkv_err[flat] = std::fabs(dk);"),
+    "dscore_err_without_out_err": (
+        "(std::fabs(st.v[i] - st.o) * xm + oerr)", "(std::fabs(st.v[i] - st.o) * xm)"),
+    "dape_err_without_abs": (
+        "my_err[win[i].ape_index] += err + std::fabs(ds);", "my_err[win[i].ape_index] += err;"),
 }
 
 
@@ -75,6 +87,7 @@ def _run_pins(lib):
     if not np.allclose(f["out_f64"][:, 0], [eval(s, env) for s in gd["expected"]["out"]],
                        rtol=1e-15):
         failed.append("golden")
+    failed += ["golden_" + m for m in golden_mass_mismatches(lib)]
     return failed
 
 

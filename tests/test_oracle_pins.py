@@ -330,6 +330,156 @@ def test_golden_hand_pack(oracle_lib):
 
 
 # ----------------------------------------------------------------------------------
+# The error masses (the parity tolerance's first-order fp32 error sizes)
+# ----------------------------------------------------------------------------------
+
+U32 = 2.0 ** -24
+
+
+def golden_mass_mismatches(lib=None):
+    """Names of the error masses of the hand-derived golden pack that the oracle (`lib`)
+    gets wrong: out_err, dkv_err, dscore_err, dape_err against closed forms in e worked
+    out by hand (tests/golden/hand_pack_r2_c2.json)."""
+    with open(os.path.join(GOLDEN, "hand_pack_r2_c2.json")) as fh:
+        gd = json.load(fh)
+    env = {"e": math.e, "__builtins__": {}}
+    for k, v in gd["definitions"].items():
+        env[k] = eval(v, env)
+    kv = ts.f32_to_bf16_bits(np.array(gd["kv"], np.float32))
+    score = ts.f32_to_bf16_bits(np.array(gd["score"], np.float32))
+    ape = np.array(gd["ape"], np.float32)
+    dout = ts.f32_to_bf16_bits(np.array(gd["dout"], np.float32))
+    cu = np.array(gd["cu_seqlens"], np.int32)
+    r, coff, d, cap = gd["ratio"], gd["coff"], gd["d"], gd["capacity"]
+    try:
+        f = oracle.fwd(kv, score, ape, cu, r, coff, d, cap, want_err=True, lib=lib)
+        b = oracle.bwd(kv, score, ape, cu, dout, r, coff, d, cap, want_err=True, lib=lib)
+    except oracle.OracleError as ex:
+        return [f"error: {ex}"]
+    em = gd["expected_error_masses"]
+    bad = []
+    if not np.allclose(f["out_err"][:, 0], [eval(x, env) for x in em["out_err"]], rtol=1e-14,
+                       atol=0):
+        bad.append("out_err")
+    for key in ("dkv_err", "dscore_err", "dape_err"):
+        want = np.array([[eval(x, env) for x in row] for row in em[key]])
+        if not np.allclose(b[key], want, rtol=1e-14, atol=0):
+            bad.append(key)
+    return bad
+
+
+def test_error_masses_golden(oracle_lib):
+    assert golden_mass_mismatches() == []
+
+
+def f32_evaluation(pack):
+    """Every window evaluated in plain float32 (numpy, one rounding per operation, the
+    sums in window order), with window membership from brute_blocks (block starts found
+    by scanning), not from the oracle. Also the fp64 weights' |p|-weighted |kv| sums."""
+    cu = [int(x) for x in pack.cu_seqlens]
+    r, coff, d, C = pack.ratio, pack.coff, pack.d, pack.C
+    kv = ts.bf16_bits_to_f32(pack.kv)
+    sc = ts.bf16_bits_to_f32(pack.score)
+    ape = pack.ape.astype(np.float32)
+    g = ts.bf16_bits_to_f32(pack.dout)
+    blocks = brute_blocks(cu, r)
+    out = np.zeros((len(blocks), d), np.float32)
+    dkv = np.zeros((pack.capacity, C), np.float32)
+    dsc = np.zeros((pack.capacity, C), np.float32)
+    terms = np.zeros((len(blocks), r, C), np.float32)  # dScore terms per block and ape entry
+    abs_mean = np.zeros((len(blocks), d))               # sum_w p_w |kv_w| in fp64
+    for o, (s, start) in enumerate(blocks):
+        pos = []
+        if coff == 2 and start - r >= cu[s]:
+            pos += [(start - r + w, 0, w) for w in range(r)]
+        pos += [(start + w, d if coff == 2 else 0, w) for w in range(r)]
+        X = np.stack([sc[t, c:c + d] + ape[w, c:c + d] for t, c, w in pos])
+        V = np.stack([kv[t, c:c + d] for t, c, w in pos])
+        M = X.max(axis=0)
+        E = np.exp(X - M)
+        Z = np.zeros(d, np.float32)
+        for e in E:
+            Z = Z + e
+        P = E / Z
+        O = np.zeros(d, np.float32)
+        for p_, v in zip(P, V):
+            O = O + p_ * v
+        out[o] = O
+        for (t, c, w), p_, v in zip(pos, P, V):
+            k = p_ * g[o]
+            dkv[t, c:c + d] = k
+            dsc[t, c:c + d] = k * (v - O)
+            terms[o, w, c:c + d] = dsc[t, c:c + d]
+        X64 = X.astype(np.float64)
+        P64 = np.exp(X64 - X64.max(axis=0))
+        P64 /= P64.sum(axis=0)
+        abs_mean[o] = (P64 * np.abs(V.astype(np.float64))).sum(axis=0)
+    dape = terms.sum(axis=0, dtype=np.float32)  # numpy's pairwise float32 sum over blocks
+    return dict(out=out, dkv=dkv, dscore=dsc, dape=dape, abs_mean=abs_mean)
+
+
+MASS_PACKS = {
+    "r4c2_d64": lambda: ts.make_custom([37, 12, 3, 29, 40], ratio=4, coff=2, d=64, pad_rows=3,
+                                       seed=1),
+    "r2c2_d64": lambda: ts.make_custom([20, 9, 31, 1], ratio=2, coff=2, d=64, seed=3),
+    "r16c1_x4": lambda: ts.make_custom([64, 50, 33], ratio=16, coff=1, d=64, pad_rows=2, seed=2,
+                                       score_scale=4.0),
+    "r64c2_x4": lambda: ts.make_custom([300, 130], ratio=64, coff=2, d=32, seed=4,
+                                       score_scale=4.0),
+    "r128c1_x4": lambda: ts.make_custom([512, 300], ratio=128, coff=1, d=16, seed=5,
+                                        score_scale=4.0),
+}
+KAPPA_F32 = 8.0  # a plain float32 evaluation stays within KAPPA_F32 * u32 * mass
+
+
+@pytest.mark.parametrize("name", sorted(MASS_PACKS))
+def test_fp32_evaluation_within_error_masses(oracle_lib, name):
+    """The masses are large enough: a plain float32 evaluation of every window (windows of
+    4 to 128 positions, sharpened scores included) differs from the fp64 result by at most
+    KAPPA_F32 * u32 * mass, element by element, for out, dKV, dScore and dAPE. (A mass that
+    drops a term, e.g. the exponent-argument factor, fails here on the long windows.)"""
+    pack = MASS_PACKS[name]()
+    f = oracle.fwd_pack(pack, want_f64=True, want_err=True)
+    b = oracle.bwd_pack(pack, want_f64=True, want_err=True, want_owners=True)
+    e = f32_evaluation(pack)
+    own = b["owners"] > 0
+    checks = [("out", e["out"], f["out_f64"], f["out_err"]),
+              ("dkv", e["dkv"][own], b["dkv_f64"][own], b["dkv_err"][own]),
+              ("dscore", e["dscore"][own], b["dscore_f64"][own], b["dscore_err"][own]),
+              ("dape", e["dape"], b["dape_f64"], b["dape_err"])]
+    for label, got, ref, mass in checks:
+        ratio = np.abs(got.astype(np.float64) - ref) / (U32 * mass + 1e-300)
+        assert ratio.max() <= KAPPA_F32, (label, float(ratio.max()))
+
+
+def test_error_masses_cover_summand_magnitudes(oracle_lib):
+    """The masses are at least the magnitudes an fp32 evaluation rounds: out_err >= the
+    weighted absolute kv sum sum_w p_w |kv_w| (so it is never below one rounding of each
+    summand); dkv_err >= |dKV|; dscore_err >= |p g| sum_w p_w |kv_w| (the output's error
+    enters through kv - out); dape_err >= the sum of |terms|; all are exactly 0 on
+    unconsumed slots."""
+    for name in ("r4c2_d64", "r16c1_x4"):
+        pack = MASS_PACKS[name]()
+        f = oracle.fwd_pack(pack, want_f64=True, want_err=True)
+        b = oracle.bwd_pack(pack, want_f64=True, want_err=True, want_owners=True)
+        e = f32_evaluation(pack)
+        assert (f["out_err"] >= e["abs_mean"] * (1 - 1e-12)).all()
+        own = b["owners"] > 0
+        assert (b["dkv_err"][own] >= np.abs(b["dkv_f64"][own])).all()
+        assert (b["dkv_err"][~own] == 0).all() and (b["dscore_err"][~own] == 0).all()
+        assert (b["dape_err"] >= b["dape_abs"]).all()
+        # dScore: every consumed slot's mass covers |p g| times its row's sum_w p_w |kv_w|
+        m = oracle.map_blocks(pack.cu_seqlens, pack.ratio, pack.total_comp)
+        g = ts.bf16_bits_to_f32(pack.dout).astype(np.float64)
+        r, d = pack.ratio, pack.d
+        for o, (s, blk, base) in enumerate(m[:8]):
+            cols = slice(d, 2 * d) if pack.coff == 2 else slice(0, d)
+            for w in range(r):
+                pg = np.abs(b["dkv_f64"][base + w, cols])
+                assert (b["dscore_err"][base + w, cols] >= pg * e["abs_mean"][o] * (1 - 1e-12)).all()
+
+
+# ----------------------------------------------------------------------------------
 # bf16 rounding against a brute-force nearest search
 # ----------------------------------------------------------------------------------
 
