@@ -274,14 +274,6 @@ csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t st
   return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
 
-// Neumaier's compensated summation step (Neumaier 1974): s + c carries the running sum
-// with the rounding error of every addition kept in c.
-__device__ __forceinline__ void neumaier_add(float& s, float& c, float x) {
-  const float t = s + x;
-  c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
-  s = t;
-}
-
 // dAPE = (accumulate ? dAPE : 0) + sum over row groups g = 0..R-1 of partial[g]. A block
 // covers 32 entries with SPLIT warps; warp k adds the contiguous row-group range
 // [k*R/SPLIT, (k+1)*R/SPLIT) (loaded kReduceBatch at a time, so the loads overlap) with

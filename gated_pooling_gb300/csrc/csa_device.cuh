@@ -252,6 +252,14 @@ __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
 }
 // An f32 pair rounded to two bf16 (nearest even) in one word.
 __device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) { return pack_bf16x2(f2_lo(v), f2_hi(v)); }
+// Neumaier's compensated summation step (Neumaier 1974): s + c carries the running sum
+// with the rounding error of every addition kept in c.
+__device__ __forceinline__ void neumaier_add(float& s, float& c, float x) {
+  const float t = s + x;
+  c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
+  s = t;
+}
+
 // max of three fp32 (sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

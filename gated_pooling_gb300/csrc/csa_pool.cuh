@@ -501,9 +501,20 @@ inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
 #ifndef CSA_STREAM_BWD_CTAS
 #define CSA_STREAM_BWD_CTAS 1
 #endif
-// Consumers plus one producer warp per CTA (and the backward's zero warp): 8 consumer
-// warps + 1 or 2 more put at most three warps on an SM sub-partition, a 168-register
-// budget per thread (no spills).
+// Consumers plus producer warps per CTA (and the backward's zero warp): 8 consumer warps
+// + 4 producer warps forward, + 3 producer warps + the zero warp backward: 12 warps, three
+// per SM sub-partition, leave 168 registers per thread (no spills; a 13th warp would cut
+// that to 128). One warp issues about one bulk copy per quarter microsecond on GB300
+// whatever its size, so the rows are dealt to several producer warps.
+#ifndef CSA_STREAM_FWD_PRODUCERS
+#define CSA_STREAM_FWD_PRODUCERS 4
+#endif
+#ifndef CSA_STREAM_BWD_PRODUCERS
+#define CSA_STREAM_BWD_PRODUCERS 3
+#endif
+constexpr int stream_producers(bool bwd) {
+  return bwd ? CSA_STREAM_BWD_PRODUCERS : CSA_STREAM_FWD_PRODUCERS;
+}
 #ifndef CSA_FWD_VEC
 #define CSA_FWD_VEC 8
 #endif
@@ -568,10 +579,12 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
   while (depth >= 3 && ring_off + std::max(depth * pl.stage_bytes, red) + (2 * depth + 1) * 8 >
                            smem_limit)
     --depth;
-  if (depth < 3) return false;
+  const int np = stream_producers(bwd);
+  depth -= depth % np;  // every slot belongs to one producer warp
+  if (depth < 3 || depth < (size_t)np) return false;
   if ((size_t)pl.slots + 2 > depth) pl.slots = (int)depth - 2;  // keep the ring ahead of the consumers
   pl.depth = (int)depth;
-  pl.threads = nc + (bwd ? 64 : 32);  // + producer warp (+ zero warp)
+  pl.threads = nc + 32 * np + (bwd ? 32 : 0);  // + producers (+ zero warp)
   pl.ape_off = (int)ape_off;
   pl.pre_off = (int)pre_off;
   pl.ring_off = (int)ring_off;

@@ -6,10 +6,11 @@
 // Same operation and zero ownership as pool_kernel (csa_pool.cuh). One CTA per SM owns a
 // contiguous range of output rows [o0, o1). Output row o is block b of segment s; its R
 // tokens are R consecutive rows of kv/score, so the block's full-width rows are ONE
-// contiguous range of R*C bf16 values. A producer warp streams, for each row of the
-// range in order, that block of kv and of score (and, backward, the dout row) into a
-// ring of shared-memory stages with 1-D bulk asynchronous copies (TMA), completing on
-// the stage's `full` mbarrier. The window of row o is the left half of stage o-1
+// contiguous range of R*C bf16 values. Producer warps stream, for each row of the range,
+// that block of kv and of score (and, backward, the dout row) into a ring of
+// shared-memory stages with 1-D bulk asynchronous copies (TMA), completing on the
+// stage's `full` mbarrier; rows are dealt round robin to the producer warps, since one
+// warp issues about one bulk copy per quarter microsecond. The window of row o is the left half of stage o-1
 // (previous block, coff=2) and the right half of stage o (own block; the whole stage at
 // coff=1), so every consumed byte crosses HBM once. A stage is released (`empty`
 // mbarrier) once rows o and o+1 have read it; ring slots and phases are running counters.
@@ -33,9 +34,10 @@
 namespace csa {
 
 template <int VEC, int NC, int R, int COFF, bool BWD>
-__global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
+__global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 0),
                                   BWD ? CSA_STREAM_BWD_CTAS : CSA_STREAM_FWD_CTAS)
     pool_stream_kernel(const PoolParams p) {
+  constexpr int NP = stream_producers(BWD);  // producer warps
   constexpr int NW = VEC / 2;               // 32-bit words (= column pairs) per chunk
   // ape values per shared-memory vector: pairs in the forward (two 8-byte reads per
   // position measured slightly faster than one 16-byte read), quads in the backward
@@ -107,13 +109,17 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
     for (int q = 0; q < NW; ++q) acc[i][q] = 0ull;
 
   if (tid >= NC) {
-    // ------------------------------ producer ------------------------------------------
-    // the producer warp's lanes issue the previous block's 2*R row copies together; lane 0
-    // then streams the stages. (lane >= 32: the backward's zero warp)
-    const int lane = tid - NC;
+    // ------------------------------ producers -----------------------------------------
+    // NP producer warps; lane 0 of warp pw streams the rows j = pw, pw + NP, ... into ring
+    // slots j mod depth (depth is a multiple of NP, so every slot has one producer). A warp
+    // has one bulk copy in issue at a time (about a quarter of a microsecond each on GB300),
+    // so several warps issuing side by side keep the copy engine busy. Warp 0's lanes first
+    // issue the previous block's 2*R row copies together. (Warp NP: the backward's zero warp.)
+    const int pw = (tid - NC) >> 5;
+    const int lane = (tid - NC) & 31;
     const uint64_t pol = l2_evict_first_policy();
-    int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
-    if (need_pre && lane < 32) {
+    if (pw == 0 && need_pre) {
+      const int s = find_segment(sB, p.S, o0);
       if (lane == 0) mbar_arrive_expect_tx(pre_bar, static_cast<uint32_t>(2 * R * d * 2));
       __syncwarp();
       if (lane < 2 * R) {
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
                        d * 2, pre_bar, pol);
       }
     }
-    if (BWD && lane >= 32) {
+    if (BWD && pw == NP) {
       // the zero warp (backward): the zeros of segments shorter than ratio and of this row
       // group's share of the padding rows, written while the consumers stream
       const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
       for (int s2 = s_lo; s2 < s_hi; ++s2) {
         const int a = sCu[s2];
         const int b = sCu[s2 + 1];
-        if (b - a < R && b > a) zero_rows<NW>(p, a, b - a, V, lane - 32, 32);
+        if (b - a < R && b > a) zero_rows<NW>(p, a, b - a, V, lane, 32);
       }
       const int64_t c_first = sCu[0];
       const int64_t c_last = sCu[p.S];
@@ -140,16 +146,17 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
       const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
       const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
       const int64_t h0 = min(q1, c_first);
-      if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, V, lane - 32, 32);
+      if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, V, lane, 32);
       const int64_t t0 = max(q0, c_first), t1 = q1;
-      if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, V, lane - 32, 32);
+      if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, V, lane, 32);
     }
-    if (lane == 0) {
+    if (pw < NP && lane == 0) {
       const int withheld = (blockIdx.x == 0 && blockIdx.y == 0) ? p.withhold_row : -1;
-      int j = 0;
-      int slot = 0;       // j % depth
-      uint32_t ph = 0;    // (j / depth) & 1
-      for (; j < nrows; ++j, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
+      int s = nrows > pw ? find_segment(sB, p.S, o0 + pw) : 0;
+      int j = pw;
+      int slot = pw;     // j % depth
+      uint32_t ph = 0;   // (j / depth) & 1
+      for (; j < nrows; j += NP) {
         if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u, p.wait_cycles)) {
           s_abort = 1;
           break;
@@ -157,26 +164,33 @@ __global__ void __launch_bounds__(NC + (BWD ? 64 : 32),
         if (*reinterpret_cast<volatile int*>(&s_abort)) break;
         const int o = o0 + j;
         s = advance_segment(sB, s, o);
-        if (j == withheld) continue;  // test hook: this stage never fills
-        const int base = sCu[s] + (o - sB[s]) * R;
-        unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_g + (BWD ? d * 2 : 0)));
-        const int64_t off = static_cast<int64_t>(base) * C;
-        bulk_load_hint(st, p.kv + off, kv_bytes, &full[slot], pol);
-        bulk_load_hint(st + kv_bytes, p.score + off, kv_bytes, &full[slot], pol);
-        if constexpr (BWD)
-          bulk_load_hint(st + stage_g, p.dout + static_cast<int64_t>(o) * d, d * 2, &full[slot], pol);
+        if (j != withheld) {  // test hook: a withheld stage never fills
+          const int base = sCu[s] + (o - sB[s]) * R;
+          unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+          mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_g + (BWD ? d * 2 : 0)));
+          const int64_t off = static_cast<int64_t>(base) * C;
+          bulk_load_hint(st, p.kv + off, kv_bytes, &full[slot], pol);
+          bulk_load_hint(st + kv_bytes, p.score + off, kv_bytes, &full[slot], pol);
+          if constexpr (BWD)
+            bulk_load_hint(st + stage_g, p.dout + static_cast<int64_t>(o) * d, d * 2, &full[slot],
+                           pol);
+        }
+        slot += NP;
+        if (slot >= p.depth) {
+          slot -= p.depth;
+          ph ^= 1u;
+        }
       }
       if ((j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) && p.dev_error != nullptr)
         *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;  // stopped early
-      // Every copy issued here lands before the CTA can exit: normally the consumers have
-      // waited for all of them already, but consumers that stop early have not. (Slots of
-      // rows before j - depth were handed back by the consumers, so their copies landed.)
-      for (int k = max(0, j - p.depth); k < j; ++k)
+      // Every copy this warp issued lands before the CTA can exit: normally the consumers
+      // have waited for all of them already, but consumers that stop early have not. (The
+      // slots of this warp's rows before j - depth were handed back, so those landed.)
+      for (int k = j - NP; k >= 0 && k >= j - p.depth; k -= NP)
         if (k != withheld)
           mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1),
                             kWaitCycles);
-      if (need_pre) mbar_wait_bounded(pre_bar, 0, kWaitCycles);
+      if (pw == 0 && need_pre) mbar_wait_bounded(pre_bar, 0, kWaitCycles);
     }
   } else {
     // ------------------------------ consumers -----------------------------------------
