@@ -21,6 +21,9 @@ PoolKernel bwd_kernel_for(const Plan& pl) {
                          : reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_BWD_GROUPS, 1, true>);
       case 8: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_BWD_GROUPS, 2, true>)
                          : reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_BWD_GROUPS, 1, true>);
+      case 16:  // 256-position windows: ratio 128 at coff 2 only
+        return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<16, long_groups(true, 256), 2, true>)
+                   : nullptr;
       default: return nullptr;
     }
   }

@@ -410,4 +410,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+
+// Ring slot bookkeeping: the producer records in shared memory which row it has armed a
+// slot's `full` barrier for, and a consumer waits (bounded) until its row is recorded
+// before it waits on the barrier's phase parity. A parity wait alone cannot tell phase k
+// from phase k - 2: a consumer that reaches row j while the slot's previous row
+// (j - depth) has not landed yet would see the barrier one phase behind and take the
+// stale phase for its own. With the row recorded, the barrier is known to be in row j's
+// phase, and the parity wait is exact.
+__device__ __forceinline__ void st_release_shared(int* p, int v) {
+  asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+// Waits until *p == v, giving up (false) after about `limit` SM clock cycles.
+__device__ __forceinline__ bool wait_shared_eq(const int* p, int v, long long limit) {
+  if (ld_acquire_shared(p) == v) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_shared(p) != v)
+    if (clock64() - t0 > limit) return false;
+  return true;
+}
+
 }  // namespace csa

@@ -21,6 +21,9 @@ PoolKernel fwd_kernel_for(const Plan& pl) {
                          : reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 1, false>);
       case 8: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 2, false>)
                          : reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 1, false>);
+      case 16:  // 256-position windows: ratio 128 at coff 2 only
+        return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<16, long_groups(false, 256), 2, false>)
+                   : nullptr;
       default: return nullptr;
     }
   }
@@ -29,10 +32,10 @@ PoolKernel fwd_kernel_for(const Plan& pl) {
     if (r == 1 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 1, 1>;
     if (r == 2 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 2, 1>;
     if (r == 4 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 4, 1>;
-    if (r == 8 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 8, 1>;
+    if (r == 8 && coff == 1) return pool_fwd_ldg_kernel<ldg_threads(8), 8, 1>;
     if (r == 1 && coff == 2) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 1, 2>;
     if (r == 2 && coff == 2) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 2, 2>;
-    if (r == 4 && coff == 2) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 4, 2>;
+    if (r == 4 && coff == 2) return pool_fwd_ldg_kernel<ldg_threads(8), 4, 2>;
     return nullptr;
   }
   if (pl.tma) {

@@ -74,7 +74,7 @@ struct PoolParams {
   int ape_off;      // byte offsets in dynamic shared memory: staged ape,
   int pre_off;      //   the block before the first row (left half),
   int ring_off;     //   the ring of stages,
-  int bar_off;      //   the full/empty mbarriers
+  int bar_off;      //   the full/empty mbarriers, then the rows the slots are armed for
   int box_rows;     // long windows: tokens per tensor box
 };
 
@@ -112,8 +112,10 @@ __device__ __forceinline__ void zero_rows(const PoolParams& p, int64_t row0, int
 
 // VEC: columns per chunk (8 forward, 4 backward). PP: window positions per thread.
 // SPLIT: windows span several position groups (P > 1).
+// (8-position backward: one CTA per SM, so that its window, weights and dAPE sums stay in
+// registers without spills)
 template <int VEC, int PP, bool BWD, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 2) pool_kernel(const PoolParams p) {
+__global__ void __launch_bounds__(kThreads, (BWD && PP >= 8) ? 1 : 2) pool_kernel(const PoolParams p) {
   constexpr int NW = VEC / 2;  // 32-bit words per chunk
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
@@ -534,6 +536,12 @@ constexpr int stream_producers(bool bwd) {
 #ifndef CSA_LDG_THREADS
 #define CSA_LDG_THREADS 512
 #endif
+// 8-position windows keep two rows of 32 words each in registers per thread: 384 threads
+// (168 registers each) instead of 512 (128 each, which spilled)
+#ifndef CSA_LDG_THREADS_W8
+#define CSA_LDG_THREADS_W8 384
+#endif
+constexpr int ldg_threads(int window) { return window >= 8 ? CSA_LDG_THREADS_W8 : CSA_LDG_THREADS; }
 #ifndef CSA_LDG_CTAS
 #define CSA_LDG_CTAS 1
 #endif
@@ -576,7 +584,7 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
   smem_limit = std::min<size_t>(smem_limit, (228 * 1024) / ctas - 1024 - 256);
   if (smem_limit <= ring_off + 64) return false;
   size_t depth = std::min<size_t>(64, (smem_limit - ring_off - 8) / (pl.stage_bytes + 16));
-  while (depth >= 3 && ring_off + std::max(depth * pl.stage_bytes, red) + (2 * depth + 1) * 8 >
+  while (depth >= 3 && ring_off + std::max(depth * pl.stage_bytes, red) + (2 * depth + 1) * 8 + depth * 4 >
                            smem_limit)
     --depth;
   const int np = stream_producers(bwd);
@@ -589,7 +597,7 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
   pl.pre_off = (int)pre_off;
   pl.ring_off = (int)ring_off;
   pl.bar_off = (int)(ring_off + std::max(depth * pl.stage_bytes, red));
-  pl.smem = (size_t)pl.bar_off + (2 * depth + 1) * 8;
+  pl.smem = (size_t)pl.bar_off + (2 * depth + 1) * 8 + depth * 4;
   *out = pl;
   return true;
 }
@@ -619,21 +627,22 @@ inline bool plan_fwd_ldg(int S, int r, int coff, int d, size_t smem_limit, Plan*
   pl.pp = coff * r;
   pl.P = 1;
   pl.V = d / 4;
-  if (pl.V > CSA_LDG_THREADS) return false;
+  const int nt = ldg_threads(coff * r);
+  if (pl.V > nt) return false;
   pl.Vs = pl.V;
   pl.K = 1;
-  pl.slots = CSA_LDG_THREADS / pl.V;
+  pl.slots = nt / pl.V;
   pl.sB_words = ((S + 1) + 3) & ~3;
   pl.ape_off = pl.sB_words * 8;
   pl.smem = (size_t)pl.ape_off + (size_t)coff * r * d * 4;
   if (pl.smem > smem_limit) return false;
-  pl.threads = CSA_LDG_THREADS;
+  pl.threads = nt;
   *out = pl;
   return true;
 }
 
-// Long-window geometry (csa_pool_long.cuh): W = coff*ratio in {16, 32, 64, 128} and d a
-// multiple of 64. A CTA slice is 64 columns per half (16 chunks of 4); a stage holds the
+// Long-window geometry (csa_pool_long.cuh): W = coff*ratio in {16, 32, 64, 128, 256} and d
+// a multiple of 64. A CTA slice is 64 columns per half (16 chunks of 4); a stage holds the
 // [W x 64] kv and score tiles (tile rows of 128 bytes, 1024-byte aligned for the 128-byte
 // swizzle; at coff=2 the own half starts at tile row ratio, a multiple of 8), the backward
 // adds the dout slice in a ring of its own. Tensor boxes (loads, and the backward's
@@ -648,9 +657,21 @@ constexpr int kLongSliceCols = 64;  // columns per half in a long-window CTA sli
 #define CSA_LONG_BWD_GROUPS 2
 #endif
 
+// Consumer groups of the long-window kernel for a window of W positions: 256-position
+// windows (ratio 128 at coff 2) have 64 KB stages, of which only two or three fit, so they
+// run one group per direction.
+constexpr int long_groups(bool bwd, int W) {
+  return W >= 256 ? 1 : (bwd ? CSA_LONG_BWD_GROUPS : CSA_LONG_FWD_GROUPS);
+}
+
+#ifndef CSA_LONG_W256
+#define CSA_LONG_W256 1  // 256-position windows on the long-window kernel (else the split kernel)
+#endif
 inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
   const int W = coff * r;
-  if (!(W == 16 || W == 32 || W == 64 || W == 128) || d % 64 != 0) return false;
+  if (!(W == 16 || W == 32 || W == 64 || W == 128 || (CSA_LONG_W256 && W == 256)) ||
+      d % 64 != 0)
+    return false;
   Plan pl;
   pl.longk = true;
   pl.coff = coff;
@@ -663,13 +684,14 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit
   pl.slots = 1;
   pl.box_rows = r;
   pl.sB_words = ((S + 1) + 3) & ~3;
-  const int ng = bwd ? CSA_LONG_BWD_GROUPS : CSA_LONG_FWD_GROUPS;
+  const int ng = long_groups(bwd, W);
   const bool ape_smem = bwd || ng > 1;  // else the forward keeps ape in registers
   const size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
   const size_t ring_off = ape_off + (ape_smem ? (size_t)16 * (W + 4) * 16 : 0);
   pl.stage_bytes = 2 * W * 128;
-  // + the dout slice and 3 mbarriers (backward), 2 mbarriers (forward)
-  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 + 24 : 16);
+  // + the dout slice (backward),
+  // + the mbarriers (3 backward, 2 forward) and the slot's armed-row word
+  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 + 24 : 16) + 4;
   if (smem_limit < ring_off + 1024 + 2 * per_stage) return false;
   const size_t depth = std::min<size_t>(16, (smem_limit - ring_off - 1024) / per_stage);
   if (depth <= (size_t)ng) return false;  // every consumer group needs a stage of its own

@@ -1,6 +1,7 @@
-// csa_pool_long.cuh -- pooling kernel for long windows (W = coff*ratio in {16, 32, 64, 128};
-// e.g. the ratio=128 coff=1 family of "Megatron-LM PR #5984", commit "add dedicated
-// ratio=128 kernels"), forward and backward, for head dims that are multiples of 64.
+// csa_pool_long.cuh -- pooling kernel for long windows (W = coff*ratio in {16, 32, 64, 128,
+// 256}; e.g. the ratio=128 family of "Megatron-LM PR #5984", commit "add dedicated
+// ratio=128 kernels", at coff 1 and 2), forward and backward, for head dims that are
+// multiples of 64.
 //
 // Same operation and zero ownership as pool_kernel (csa_pool.cuh). A CTA owns a slice of 64
 // columns per half and a contiguous range of output rows. For each row a producer warp
@@ -88,7 +89,9 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   constexpr int NCT = NG * kThreads;  // consumer threads
   static_assert(NG >= 1 && (!BWD || NG <= 2), "the dAPE combine handles two groups");
   constexpr bool kApReg = !BWD && NG == 1;
-  constexpr bool kRecomp = BWD && NG > 1;
+  // the backward recomputes the softmax terms from the staged tile in each pass when two
+  // groups share the registers, or when a lane owns 16 positions (256-position windows)
+  constexpr bool kRecomp = BWD && (NG > 1 || PP >= 16);
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   __shared__ int s_abort;
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(gring + (BWD ? p.depth * kLongSlice * 2 : 0));
   uint64_t* empty = full + p.depth;
   uint64_t* done = empty + p.depth;  // backward: a group has written the stage's gradients
+  int* slot_row = reinterpret_cast<int*>(full + (BWD ? 3 : 2) * p.depth);  // armed rows
 
   const int tid = threadIdx.x;
   // mbarriers, one per thread, before the map is read (their set-up does not depend on
@@ -116,6 +120,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       fence_proxy_async_smem();
     }
     if (tid == 0) s_abort = 0;
+    if (tid < p.depth) slot_row[tid] = -1;
   }
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
@@ -213,6 +218,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         const int base = sCu[s] + b * r;
         const bool has_prev = two && b >= 1;
         unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+        st_release_shared(&slot_row[slot], j);  // the slot's barrier is now in row j's phase
         const int boxes = has_prev ? 2 : 1;
         mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(boxes * r * 128 * 2 +
                                                                  (BWD ? kLongSlice * 2 : 0)));
@@ -305,7 +311,9 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     const int b = o - sB[s];
     const int base = sCu[s] + b * r;
     const bool has_prev = two && b >= 1;
-    const bool ok = mbar_wait_bounded(&full[slot], ph, p.wait_cycles);
+    // row j's phase of its slot (see wait_shared_eq), then that phase's completion
+    const bool ok = wait_shared_eq(&slot_row[slot], j, p.wait_cycles) &&
+                    mbar_wait_bounded(&full[slot], ph, p.wait_cycles);
     if (!__all_sync(0xFFFFFFFFu, ok)) {  // a copy wait ran out: stop, and say so
       s_abort = 1;
       if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;

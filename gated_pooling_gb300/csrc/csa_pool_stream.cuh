@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.depth;
   uint64_t* pre_bar = empty + p.depth;
+  int* slot_row = reinterpret_cast<int*>(pre_bar + 1);  // row each slot is armed for
 
   const int tid = threadIdx.x;
   const int d = p.d, C = p.C, V = p.V;
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
     else mbar_init(pre_bar, 1);
     fence_proxy_async_smem();
   }
+  if (tid < p.depth) slot_row[tid] = -1;
   if (tid == 0) s_abort = 0;
 
   // (the block prefix ends with a barrier: the mbarriers are ready after it)
@@ -167,6 +169,7 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
         if (j != withheld) {  // test hook: a withheld stage never fills
           const int base = sCu[s] + (o - sB[s]) * R;
           unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
+          st_release_shared(&slot_row[slot], j);  // the slot's barrier is now in row j's phase
           mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_g + (BWD ? d * 2 : 0)));
           const int64_t off = static_cast<int64_t>(base) * C;
           bulk_load_hint(st, p.kv + off, kv_bytes, &full[slot], pol);
@@ -231,7 +234,9 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
         const int cs = sCu[s];
         const int base = cs + b * R;
         const bool has_prev = TWO && b >= 1;
-        bool ok = mbar_wait_bounded(&full[slot], ph, p.wait_cycles);
+        // row j's phase of its slot (see wait_shared_eq), then that phase's completion
+        bool ok = wait_shared_eq(&slot_row[slot], j, p.wait_cycles) &&
+                  mbar_wait_bounded(&full[slot], ph, p.wait_cycles);
         // kv chunk of the own block's first token; score sits kv_bytes further, rows are C2
         // bytes apart. The previous block (coff=2) uses the same layout (its own stage, or
         // the block fetched before the first row).
@@ -244,7 +249,8 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
             ok = ok && mbar_wait_bounded(pre_bar, 0, p.wait_cycles);
             prev_kv = pre + c0 * 2;
           } else {
-            ok = ok && mbar_wait_bounded(&full[pslot], pph, p.wait_cycles);
+            ok = ok && wait_shared_eq(&slot_row[pslot], j - 1, p.wait_cycles) &&
+                 mbar_wait_bounded(&full[pslot], pph, p.wait_cycles);
             prev_kv = stages + static_cast<size_t>(pslot) * p.stage_bytes + c0 * 2;
           }
         }
@@ -407,9 +413,20 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
             }
           }
         }
-        // release the own stage and (coff=2) the previous one, which row o-1 also read
+        // release the own stage and (coff=2) the previous one, which row o-1 also read. A
+        // segment's first block has not read the previous stage and so has not seen it
+        // armed for row j-1: with several producer warps row j can be armed before row j-1,
+        // and an arrival on the previous slot's `empty` barrier before that would count
+        // toward the slot's earlier phase. So it waits for row j-1's arming first.
         mbar_arrive(&empty[slot]);
-        if (TWO && j >= 1) mbar_arrive(&empty[pslot]);
+        if (TWO && j >= 1) {
+          if (!has_prev && !wait_shared_eq(&slot_row[pslot], j - 1, p.wait_cycles)) {
+            s_abort = 1;
+            if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
+            break;
+          }
+          mbar_arrive(&empty[pslot]);
+        }
         slot += p.slots;
         if (slot >= p.depth) {
           slot -= p.depth;

@@ -67,6 +67,11 @@ def small_packs():
         "r64c2_d64": ts.make_custom([260, 70, 10], ratio=64, coff=2, d=64, pad_rows=3, seed=25,
                                     score_scale=4.0),
         "r16c1_d64": ts.make_custom([50, 16, 5], ratio=16, coff=1, d=64, pad_rows=0, seed=26),
+        # 256-position windows (ratio 128 x coff 2) on the long-window kernel: first blocks,
+        # short segment, tail, two column slices
+        "r128c2_d128": ts.make_custom([400, 256, 127, 300], ratio=128, coff=2, d=128,
+                                      pad_rows=3, seed=27, score_scale=4.0),
+        "r128c2_d64": ts.make_custom([520, 128], ratio=128, coff=2, d=64, pad_rows=1, seed=28),
         # generic kernel: head dims that are not a multiple of 8 (several column slices,
         # windows up to its 256-position limit)
         "g_d65_r4c2": ts.make_custom([37, 12, 3, 20], ratio=4, coff=2, d=65, pad_rows=3, seed=30),

@@ -148,6 +148,9 @@ SPECS: Dict[str, PackSpec] = {
     # The pages' two other ratio=4 coff=2 shapes, kept as context rows for the bench.
     "3x8192_d128": PackSpec("3x8192_d128", [8192] * 3, ratio=4, coff=2, d=128),
     "1x8192_d512": PackSpec("1x8192_d512", [8192], ratio=4, coff=2, d=512),
+    # The pages' ratio=128 coff=2 d=128 example (65k tokens), as eight 8192-token
+    # sequences, kept as a context row for the long-window kernel's 256-position windows.
+    "r128c2_d128": PackSpec("r128c2_d128", [8192] * 8, ratio=128, coff=2, d=128),
 }
 
 HEADLINE = "3x8192_d512"
