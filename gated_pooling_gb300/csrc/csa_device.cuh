@@ -210,6 +210,16 @@ __device__ __forceinline__ int advance_segment(const int* sB, int s, int o) {
   return s;
 }
 
+// First s in [lo, hi) with sB[s] > v (hi if none).
+__device__ __forceinline__ int upper_bound_prefix(const int* sB, int lo, int hi, int v) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (sB[mid] <= v) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
 // First s in [lo, hi) with sB[s] >= v (hi if none).
 __device__ __forceinline__ int lower_bound_prefix(const int* sB, int lo, int hi, int v) {
   while (lo < hi) {

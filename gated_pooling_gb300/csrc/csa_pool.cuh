@@ -88,16 +88,18 @@ __device__ __forceinline__ void publish_status(const PoolParams& p, int TC) {
 }
 
 // Zeroes rows [row0, row0+nrows) of dKV and dScore over this CTA's column slice (both
-// halves at coff=2). Cooperative over the whole CTA.
+// halves at coff=2, or only the first half with `first_half_only`). Cooperative over the
+// threads t0, t0 + nt, ... (the whole CTA by default).
 template <int NW>
 __device__ __forceinline__ void zero_rows(const PoolParams& p, int64_t row0, int64_t nrows,
-                                          int slice_chunks, int t0 = -1, int nt = 0) {
+                                          int slice_chunks, int t0 = -1, int nt = 0,
+                                          bool first_half_only = false) {
   constexpr int VEC = 2 * NW;
   if (t0 < 0) {
     t0 = threadIdx.x;
     nt = blockDim.x;
   }
-  const int per_row = slice_chunks * p.coff;
+  const int per_row = slice_chunks * (first_half_only ? 1 : p.coff);
   const int64_t items = nrows * per_row;
   for (int64_t it = t0; it < items; it += nt) {
     const int64_t row = row0 + it / per_row;

@@ -12,8 +12,9 @@
 // backward writes each slot's dKV and dScore over the kv and score values it has consumed in
 // the stage (every slot has exactly one reader and writer), and a store warp copies the
 // finished tiles out with tensor-map bulk stores, whole 128-byte tile rows at a time, before
-// it hands the stage back to the producer. A zero warp writes the zeros of short segments
-// and of the rows outside [cu[0], cu[S]) meanwhile.
+// it hands the stage back to the producer. A zero warp writes meanwhile the zeros of short
+// segments, of the rows outside [cu[0], cu[S]), and of the segments whose last block is a
+// row of the CTA (that block's own first-half columns at coff=2, and the segment's tail).
 //
 // Consumers are NG groups of 8 warps; group h takes the rows h, h+NG, ... of the CTA's
 // range (more groups keep more warps in flight where registers allow). Warp wi of a
@@ -187,6 +188,19 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         const int a = sCu[s], b = sCu[s + 1];
         if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, kLongSlice / VEC, zt, 32);
       }
+      // segments whose last block is a row of this group (sB[s+1] - 1 in [o0, o1)): the
+      // first-half columns of that block's own tokens (coff=2; no next block reads them)
+      // and the segment's tail tokens
+      const int t_lo = upper_bound_prefix(sB, 1, p.S + 1, o0);
+      const int t_hi = upper_bound_prefix(sB, t_lo, p.S + 1, o1);
+      for (int t = t_lo; t < t_hi; ++t) {
+        const int s = t - 1;
+        const int n = sB[t] - sB[s];
+        if (n < 1) continue;
+        const int cs = sCu[s], ce = sCu[t];
+        if (two) zero_rows<NW>(p, cs + (n - 1) * r, r, kLongSlice / VEC, zt, 32, true);
+        if (ce > cs + n * r) zero_rows<NW>(p, cs + n * r, ce - cs - n * r, kLongSlice / VEC, zt, 32);
+      }
       const int64_t c_first = sCu[0];
       const int64_t c_last = sCu[p.S];
       const int64_t npad = c_first + (p.capacity - c_last);
@@ -285,9 +299,15 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   }
   if constexpr (!kApReg) asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // ape staged
 
+  // (16 positions per lane: the shared-memory reads are volatile, so that the compiler does
+  // not hoist all positions' reads ahead and run out of registers)
   auto ape_at = [&](const int i, const int w) -> float4 {
     if constexpr (kApReg) {
       return make_float4(ap[i][0], ap[i][1], ap[i][2], ap[i][3]);
+    } else if constexpr (PP >= 16) {
+      const uint4 t = lds128_fresh(sAp + w);
+      return make_float4(__uint_as_float(t.x), __uint_as_float(t.y), __uint_as_float(t.z),
+                         __uint_as_float(t.w));
     } else {
       return sAp[w];
     }
@@ -299,6 +319,9 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
 #pragma unroll
     for (int c = 0; c < VEC; ++c) acc[i][c] = 0.f;
 
+  // this thread's tile offset for position pg + 16 i is sw0 + 2048 i: the swizzle depends on
+  // the tile row only through its low three bits, which are those of pg
+  const int sw0 = swz(pg, wi) + ch * 8;
   int s = nrows > grp ? find_segment(sB, p.S, o0 + grp) : 0;
   // stage of row j and its phase parity, advanced by NG rows per iteration (NG < depth):
   // the new slot is below NG exactly when it wrapped
@@ -327,7 +350,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     // keeping x' (and e) in registers.
     auto x_at = [&](const int i, const int w, float (&x)[VEC]) {
       uint32_t sw[NW];
-      lds_words<NW>(sw, st + kTile + swz(w, wi) + ch * 8);
+      if constexpr (PP >= 16) lds_words_fresh<NW>(sw, st + kTile + sw0 + i * 2048);
+      else lds_words<NW>(sw, st + kTile + sw0 + i * 2048);
       const float4 a4 = ape_at(i, w);
       x[0] = fmaf(bf16_lo(sw[0]), kLog2e, a4.x);
       x[1] = fmaf(bf16_hi(sw[0]), kLog2e, a4.y);
@@ -364,7 +388,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       const int w = pg + 16 * i;
       if (two && w < r && !has_prev) continue;
       uint32_t kw[NW];
-      lds_words<NW>(kw, st + swz(w, wi) + ch * 8);
+      if constexpr (PP >= 16) lds_words_fresh<NW>(kw, st + sw0 + i * 2048);
+      else lds_words<NW>(kw, st + sw0 + i * 2048);
       const float v[VEC] = {bf16_lo(kw[0]), bf16_hi(kw[0]), bf16_lo(kw[1]), bf16_hi(kw[1])};
       float x[VEC];
       if constexpr (kRecomp) {
@@ -418,7 +443,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         const bool prev = two && w < r;
         if (prev && !has_prev) continue;
         uint32_t kw[NW];
-        lds_words_fresh<NW>(kw, st + swz(w, wi) + ch * 8);
+        lds_words_fresh<NW>(kw, st + sw0 + i * 2048);
         const float v[VEC] = {bf16_lo(kw[0]), bf16_hi(kw[0]), bf16_lo(kw[1]), bf16_hi(kw[1])};
         float ei[VEC];
         if constexpr (kRecomp) {
@@ -438,30 +463,11 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
           acc[i][c] += t[c];
         }
         // dKV and dScore replace the kv and score values of this slot in the stage
-        sts_words2(st + swz(w, wi) + ch * 8, pack_bf16x2(kk[0], kk[1]), pack_bf16x2(kk[2], kk[3]));
-        sts_words2(st + kTile + swz(w, wi) + ch * 8, pack_bf16x2(t[0], t[1]),
+        sts_words2(st + sw0 + i * 2048, pack_bf16x2(kk[0], kk[1]), pack_bf16x2(kk[2], kk[3]));
+        sts_words2(st + kTile + sw0 + i * 2048, pack_bf16x2(t[0], t[1]),
                    pack_bf16x2(t[2], t[3]));
       }
-      const int n = sB[s + 1] - sB[s];
-      if (b == n - 1) {  // zeros owned by a segment's last block, spread over the lanes
-        const int64_t cz = col0 + cl;
-        if (two)  // the own block's first-half columns: no next block reads them
-          for (int k = pg; k < r; k += 16) {
-            const int64_t offz = static_cast<int64_t>(base + k) * C + cz;
-            store_zero<NW>(p.dkv + offz);
-            store_zero<NW>(p.dscore + offz);
-          }
-        const int ce = sCu[s + 1];
-        for (int t = sCu[s] + n * r + pg; t < ce; t += 16) {  // the segment's tail
-          const int64_t offz = static_cast<int64_t>(t) * C + cz;
-          store_zero<NW>(p.dkv + offz);
-          store_zero<NW>(p.dscore + offz);
-          if (two) {
-            store_zero<NW>(p.dkv + offz + d);
-            store_zero<NW>(p.dscore + offz + d);
-          }
-        }
-      }
+      // (the zeros owned by a segment's last block are written by the zero warp)
     }
     if constexpr (BWD) {
       fence_proxy_async_smem();  // the stage's new contents, to the bulk-store engine
