@@ -45,11 +45,14 @@ L2_FLUSH_BYTES = 256 << 20
 # not the target). vs_baseline = our GB/s / (the same algorithmic bytes / that time).
 PAGE_FWD_BWD_US = {"1x8192_d128": 4.5 + 12.8, "3x8192_d128": 10.0 + 22.2,
                    "1x8192_d512": 12.4 + 22.8, "3x8192_d512": 35.0 + 66.0}
-# DRAM bytes per backward call (pool kernel + reduction), from one ncu capture of the
-# current kernels (the summaries are kept with the profiles): DRAM reads plus the bytes
-# the kernels write into L2 (all of which reach DRAM). Re-measured whenever a kernel
-# changes; absent (null) until then.
-ROOFLINE_TRAFFIC = {}
+# DRAM bytes per backward call, from one ncu capture of the current pooling kernel (the
+# summaries are kept with the profiles): its DRAM reads (dram__bytes_read.sum) plus the
+# bytes it writes into L2 (lts__t_sectors_srcunit_tex_op_write.sum x 32, all of which
+# reach DRAM, also the part still dirty in L2 when the kernel ends), plus the dAPE partials
+# the reduction kernel reads (row groups x ratio x coff*d x 4 bytes). Re-measured whenever
+# a kernel changes.
+ROOFLINE_TRAFFIC = {"3x8192_d512": 108.269312e6 + 3223553 * 32 + 152 * 4 * 1024 * 4,
+                    "long_r128_d512": 136.684032e6 + 4349953 * 32 + 19 * 128 * 512 * 4}
 
 
 # ----------------------------------------------------------------------------------
@@ -258,25 +261,28 @@ def run_ours(args, rank, world, local_rank):
         bwd(sets[k % n_sets])
     st1.record(stream)
     bracket()
-    # the per-call split (and the roofline's backward-call time): the steady pass again,
-    # with events between the calls (an event between the two calls keeps the backward
-    # from starting early, so the split's sum is a little above the steady step)
-    ev = [new_events(3) for _ in range(args.steps)]
-    for k in range(args.steps):
-        ev[k][0].record(stream)
-        fwd(sets[k % n_sets])
-        ev[k][1].record(stream)
-        bwd(sets[k % n_sets])
-        ev[k][2].record(stream)
-    bracket()
+    # the per-call split (and the roofline's backward-call time): K back-to-back forward
+    # calls, then K back-to-back backward calls, over the rotated sets, events at the ends
+    # only (an event between two calls would keep the second from launching early, which
+    # back-to-back calls do)
+    def steady_only(call):
+        a, b = new_events(2)
+        bracket()
+        a.record(stream)
+        for k in range(args.steps):
+            call(sets[k % n_sets])
+        b.record(stream)
+        bracket()
+        return a.elapsed_time(b)
+
+    fwd_pass_ms = steady_only(fwd)
+    bwd_pass_ms = steady_only(bwd)
     clocks = sampler.stop() if rank == 0 else None
     if int(err.item()) != 0:
         raise RuntimeError(f"device error {int(err.item())}")
     step_ms = [sev[k][0].elapsed_time(sev[k][1]) for k in range(args.steps)]
-    fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
-    bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
     total_ms, steady_total, fwd_total, bwd_total = max_over_ranks(
-        [sum(step_ms), st0.elapsed_time(st1), sum(fwd_ms), sum(bwd_ms)], device=dev)
+        [sum(step_ms), st0.elapsed_time(st1), fwd_pass_ms, bwd_pass_ms], device=dev)
     flushed_ms = total_ms / args.steps
     steady_ms = steady_total / args.steps
     ms_step = max(flushed_ms, steady_ms)  # the lower throughput is the headline
@@ -337,7 +343,7 @@ def run_ours(args, rank, world, local_rank):
                           + (f"(> 2x the {l2 >> 20} MiB L2)" if n_sets * set_bytes(base) > 2 * l2
                              else f"(together smaller than the {l2 >> 20} MiB L2: this pass "
                                   f"runs from L2)")
-                          + ", no flush; per-call times from the steady pass"),
+                          + ", no flush; per-call times from steady passes of one call kind"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "flushed": {"us_per_step": round(flushed_ms * 1e3, 2),
                     "gbs_per_gpu": round(per_gpu(flushed_ms), 1)},
@@ -348,10 +354,8 @@ def run_ours(args, rank, world, local_rank):
         "fwd_plus_bwd_calls_us": round(fwd_us + bwd_us, 2),
         "graph_fwd_bwd_us": graph_us,
         "fwd_bytes": fwd_b, "bwd_bytes": bwd_b,
-        "fwd_us_median": round(1e3 * float(np.median(fwd_ms)), 2),
-        "fwd_us_min": round(1e3 * min(fwd_ms), 2),
-        "bwd_us_median": round(1e3 * float(np.median(bwd_ms)), 2),
-        "bwd_us_min": round(1e3 * min(bwd_ms), 2),
+        "flushed_step_us_median": round(1e3 * float(np.median(step_ms)), 2),
+        "flushed_step_us_min": round(1e3 * min(step_ms), 2),
         "fwd_gbs": round(fwd_b / (fwd_us * 1e-6) / 1e9, 1), "bwd_gbs": round(bwd_gbs, 1),
         "frac_of_measured_hbm": round(value / world / peak, 4),
         "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),

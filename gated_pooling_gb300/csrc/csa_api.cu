@@ -221,6 +221,7 @@ PoolParams base_params(const Plan& pl, const void* kv, const void* score, const 
   p.ring_off = pl.ring_off;
   p.bar_off = pl.bar_off;
   p.box_rows = pl.box_rows;
+  p.np = pl.np;
   p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
   p.withhold_row = g_withhold_row.load(std::memory_order_relaxed);
   return p;
@@ -291,7 +292,8 @@ __global__ void __launch_bounds__(kReduceCols * SPLIT)
                        int accumulate, const int32_t* __restrict__ status) {
   constexpr int kReduceSplit = SPLIT;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return;
+  // read with the partials (only the final write depends on it)
+  const int32_t call_status = *reinterpret_cast<const volatile int32_t*>(status);
   __shared__ float s_sum[kReduceSplit][kReduceCols];
   __shared__ float s_cmp[kReduceSplit][kReduceCols];
   const int lane = threadIdx.x % kReduceCols;
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kReduceCols * SPLIT)
     }
   }
   __syncthreads();
-  if (k == 0 && e < n) {
+  if (k == 0 && e < n && call_status == 0) {
     float t = 0.f, tc = 0.f;
     if (accumulate) neumaier_add(t, tc, dape[e]);
     neumaier_add(t, tc, s_sum[0][lane]);

@@ -29,13 +29,20 @@ PoolKernel bwd_kernel_for(const Plan& pl) {
   }
   if (pl.tma) {
     const int r = pl.pp / pl.coff, coff = pl.coff;
-    if (r == 1 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 1, 1, true>;
-    if (r == 2 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 2, 1, true>;
-    if (r == 4 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 4, 1, true>;
-    if (r == 8 && coff == 1) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 8, 1, true>;
-    if (r == 1 && coff == 2) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 1, 2, true>;
-    if (r == 2 && coff == 2) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 2, 2, true>;
-    if (r == 4 && coff == 2) return pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, 4, 2, true>;
+    // one producer warp or all of them (the plan's np)
+#define CSA_STREAM_PICK(RR, CC)                                                              \
+  if (r == RR && coff == CC)                                                                 \
+    return pl.np == 1 ? pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, RR, CC, true, 1>             \
+                      : pool_stream_kernel<CSA_BWD_VEC, CSA_BWD_CONSUMERS, RR, CC, true,                \
+                                           stream_producers(true)>;
+    CSA_STREAM_PICK(1, 1)
+    CSA_STREAM_PICK(2, 1)
+    CSA_STREAM_PICK(4, 1)
+    CSA_STREAM_PICK(8, 1)
+    CSA_STREAM_PICK(1, 2)
+    CSA_STREAM_PICK(2, 2)
+    CSA_STREAM_PICK(4, 2)
+#undef CSA_STREAM_PICK
     return nullptr;
   }
   if (pl.vec != 4) return nullptr;

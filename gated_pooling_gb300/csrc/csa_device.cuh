@@ -402,19 +402,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Non-blocking test of the phase with `parity` of `bar`.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
 // Waits for the phase with `parity` of `bar` to complete, giving up after about `limit`
 // SM clock cycles (returns false then). No wait in this library is unbounded. The
 // pipeline waits take the call's limit (PoolParams::wait_cycles, kWaitCycles unless a
@@ -430,14 +417,33 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// Copies in flight when a CTA stops early. A CTA must not exit while a bulk copy into its
+// shared memory is in flight. On the normal path its consumers wait for every copy, so
+// the producers leave without waiting. A thread whose wait ran out stops the pipeline
+// (stop_pipeline: sets the CTA's stop word), and then the copies already issued must still
+// land. A producer that is done publishes how far it issued and then reads the stop word
+// (producer_sees_stop); a stopping thread sets the stop word and then reads the published
+// counts. Each side fences (sequentially consistent, CTA scope) between its store and its
+// load, so at least one of them sees the other's store: a producer that sees the stop
+// waits for its own copies, and a stopping thread that sees a producer's count waits for
+// that producer's copies. (A producer whose count is not published yet sees the stop.)
+__device__ __forceinline__ bool producer_sees_stop(int* issued_word, int issued, int* stop) {
+  *reinterpret_cast<volatile int*>(issued_word) = issued;
+  __threadfence_block();
+  return *reinterpret_cast<volatile int*>(stop) != 0;
+}
+__device__ __forceinline__ void stop_pipeline(int* stop, int32_t* dev_error) {
+  *reinterpret_cast<volatile int*>(stop) = 1;
+  if (dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(dev_error) = 3;  // timeout
+  __threadfence_block();
+}
+__device__ __forceinline__ int read_issued(const int* issued_word) {
+  return *reinterpret_cast<const volatile int*>(issued_word);
+}
 
-// Ring slot bookkeeping: the producer records in shared memory which row it has armed a
-// slot's `full` barrier for, and a consumer waits (bounded) until its row is recorded
-// before it waits on the barrier's phase parity. A parity wait alone cannot tell phase k
-// from phase k - 2: a consumer that reaches row j while the slot's previous row
-// (j - depth) has not landed yet would see the barrier one phase behind and take the
-// stale phase for its own. With the row recorded, the barrier is known to be in row j's
-// phase, and the parity wait is exact.
+
+// Release store / acquire load of a shared-memory word (CTA scope): the row a ring slot
+// was last armed for, written by the producer warp that armed it.
 __device__ __forceinline__ void st_release_shared(int* p, int v) {
   asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
@@ -446,12 +452,13 @@ __device__ __forceinline__ int ld_acquire_shared(const int* p) {
   asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
   return v;
 }
-// Waits until *p == v, giving up (false) after about `limit` SM clock cycles.
-__device__ __forceinline__ bool wait_shared_eq(const int* p, int v, long long limit) {
+// Waits until *p == v; gives up (false) when *stop is set or after about `limit` cycles.
+__device__ __forceinline__ bool wait_shared_eq(const int* p, int v, const int* stop,
+                                               long long limit) {
   if (ld_acquire_shared(p) == v) return true;
   const long long t0 = clock64();
   while (ld_acquire_shared(p) != v)
-    if (clock64() - t0 > limit) return false;
+    if (*reinterpret_cast<const volatile int*>(stop) != 0 || clock64() - t0 > limit) return false;
   return true;
 }
 

@@ -40,13 +40,20 @@ PoolKernel fwd_kernel_for(const Plan& pl) {
   }
   if (pl.tma) {
     const int r = pl.pp / pl.coff, coff = pl.coff;
-    if (r == 1 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 1, 1, false>;
-    if (r == 2 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 2, 1, false>;
-    if (r == 4 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 4, 1, false>;
-    if (r == 8 && coff == 1) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 8, 1, false>;
-    if (r == 1 && coff == 2) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 1, 2, false>;
-    if (r == 2 && coff == 2) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 2, 2, false>;
-    if (r == 4 && coff == 2) return pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, 4, 2, false>;
+    // one producer warp or all of them (the plan's np)
+#define CSA_STREAM_PICK(RR, CC)                                                              \
+  if (r == RR && coff == CC)                                                                 \
+    return pl.np == 1 ? pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, RR, CC, false, 1>             \
+                      : pool_stream_kernel<CSA_FWD_VEC, CSA_FWD_CONSUMERS, RR, CC, false,                \
+                                           stream_producers(false)>;
+    CSA_STREAM_PICK(1, 1)
+    CSA_STREAM_PICK(2, 1)
+    CSA_STREAM_PICK(4, 1)
+    CSA_STREAM_PICK(8, 1)
+    CSA_STREAM_PICK(1, 2)
+    CSA_STREAM_PICK(2, 2)
+    CSA_STREAM_PICK(4, 2)
+#undef CSA_STREAM_PICK
     return nullptr;
   }
   if (pl.vec != 8) return nullptr;

@@ -74,8 +74,10 @@ struct PoolParams {
   int ape_off;      // byte offsets in dynamic shared memory: staged ape,
   int pre_off;      //   the block before the first row (left half),
   int ring_off;     //   the ring of stages,
-  int bar_off;      //   the full/empty mbarriers, then the rows the slots are armed for
+  int bar_off;      //   the mbarriers (full [(np+1) depth], empty [depth], the previous
+                    //   block's), then the rows the slots were armed for (np > 1)
   int box_rows;     // long windows: tokens per tensor box
+  int np;           // block-streaming kernel: producer warps that stream rows
 };
 
 // Backward: CTA (0, 0) records in the workspace's status word whether the call's
@@ -466,6 +468,7 @@ struct Plan {
   int box_rows = 0;    // long windows: tokens per tensor box
   int coff = 0;
   int threads = kThreads;
+  int np = 1;  // block-streaming kernel: producer warps that stream rows
   int depth = 0, stage_bytes = 0, ape_off = 0, pre_off = 0, ring_off = 0, bar_off = 0;
 };
 
@@ -509,12 +512,16 @@ inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
 // + 4 producer warps forward, + 3 producer warps + the zero warp backward: 12 warps, three
 // per SM sub-partition, leave 168 registers per thread (no spills; a 13th warp would cut
 // that to 128). One warp issues about one bulk copy per quarter microsecond on GB300
-// whatever its size, so the rows are dealt to several producer warps.
+// whatever its size, so the rows of stages below CSA_STREAM_ONE_PRODUCER_BYTES are dealt
+// to several producer warps; larger stages keep one.
 #ifndef CSA_STREAM_FWD_PRODUCERS
 #define CSA_STREAM_FWD_PRODUCERS 4
 #endif
 #ifndef CSA_STREAM_BWD_PRODUCERS
 #define CSA_STREAM_BWD_PRODUCERS 3
+#endif
+#ifndef CSA_STREAM_ONE_PRODUCER_BYTES
+#define CSA_STREAM_ONE_PRODUCER_BYTES (8 * 1024)
 #endif
 constexpr int stream_producers(bool bwd) {
   return bwd ? CSA_STREAM_BWD_PRODUCERS : CSA_STREAM_FWD_PRODUCERS;
@@ -585,21 +592,26 @@ inline bool plan_stream(bool bwd, int S, int r, int coff, int d, size_t smem_lim
   const int ctas = bwd ? CSA_STREAM_BWD_CTAS : CSA_STREAM_FWD_CTAS;
   smem_limit = std::min<size_t>(smem_limit, (228 * 1024) / ctas - 1024 - 256);
   if (smem_limit <= ring_off + 64) return false;
-  size_t depth = std::min<size_t>(64, (smem_limit - ring_off - 8) / (pl.stage_bytes + 16));
-  while (depth >= 3 && ring_off + std::max(depth * pl.stage_bytes, red) + (2 * depth + 1) * 8 + depth * 4 >
+  // one producer warp for stages of 8 KB or more (it keeps the copy engine busy on its
+  // own; more warps measured slower there), all of them for smaller stages
+  const int np = pl.stage_bytes >= CSA_STREAM_ONE_PRODUCER_BYTES ? 1 : stream_producers(bwd);
+  // per stage: the stage, np + 1 full barriers, the empty barrier (+ the armed-row word)
+  const size_t per_slot = (size_t)(np + 2) * 8 + (np > 1 ? 4 : 0);
+  size_t depth = std::min<size_t>(64, (smem_limit - ring_off - 8) / (pl.stage_bytes + per_slot));
+  while (depth >= 3 && ring_off + std::max(depth * pl.stage_bytes, red) + depth * per_slot + 8 >
                            smem_limit)
     --depth;
-  const int np = stream_producers(bwd);
   depth -= depth % np;  // every slot belongs to one producer warp
   if (depth < 3 || depth < (size_t)np) return false;
   if ((size_t)pl.slots + 2 > depth) pl.slots = (int)depth - 2;  // keep the ring ahead of the consumers
   pl.depth = (int)depth;
+  pl.np = np;
   pl.threads = nc + 32 * np + (bwd ? 32 : 0);  // + producers (+ zero warp)
   pl.ape_off = (int)ape_off;
   pl.pre_off = (int)pre_off;
   pl.ring_off = (int)ring_off;
   pl.bar_off = (int)(ring_off + std::max(depth * pl.stage_bytes, red));
-  pl.smem = (size_t)pl.bar_off + (2 * depth + 1) * 8 + depth * 4;
+  pl.smem = (size_t)pl.bar_off + depth * per_slot + 8;  // + the previous block's barrier
   *out = pl;
   return true;
 }
@@ -691,9 +703,8 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit
   const size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
   const size_t ring_off = ape_off + (ape_smem ? (size_t)16 * (W + 4) * 16 : 0);
   pl.stage_bytes = 2 * W * 128;
-  // + the dout slice (backward),
-  // + the mbarriers (3 backward, 2 forward) and the slot's armed-row word
-  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 + 24 : 16) + 4;
+  // + the dout slice and 4 mbarriers (backward: two full, empty, done), 3 (forward)
+  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 + 32 : 24);
   if (smem_limit < ring_off + 1024 + 2 * per_stage) return false;
   const size_t depth = std::min<size_t>(16, (smem_limit - ring_off - 1024) / per_stage);
   if (depth <= (size_t)ng) return false;  // every consumer group needs a stage of its own

@@ -96,32 +96,39 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   __shared__ int s_abort;
+  __shared__ int s_issued;  // the finished producer's row count (-1: not finished)
   int* sB = reinterpret_cast<int*>(smem);
   int* sCu = sB + p.sB_words;
   // stages start on a 1024-byte boundary (the swizzle pattern); the plan reserves the slack
   unsigned char* stages =
       smem + p.ring_off + ((1024u - (smem_addr(smem + p.ring_off) & 1023u)) & 1023u);
   unsigned char* gring = stages + static_cast<size_t>(p.depth) * p.stage_bytes;  // dout
+  // row j's stage is slot j mod depth and its `full` barrier full[j mod 2 depth]: the
+  // producer arms rows in order, so a group at row j, having seen row j - NG land, knows
+  // row j - depth was armed, which waited until slot j - 2 depth was handed back; that row
+  // has landed, so a phase-parity wait on full[j mod 2 depth] is exact (with depth
+  // barriers, a slow copy of row j - depth would alias row j's phase)
   uint64_t* full = reinterpret_cast<uint64_t*>(gring + (BWD ? p.depth * kLongSlice * 2 : 0));
-  uint64_t* empty = full + p.depth;
+  uint64_t* empty = full + 2 * p.depth;
   uint64_t* done = empty + p.depth;  // backward: a group has written the stage's gradients
-  int* slot_row = reinterpret_cast<int*>(full + (BWD ? 3 : 2) * p.depth);  // armed rows
 
   const int tid = threadIdx.x;
   // mbarriers, one per thread, before the map is read (their set-up does not depend on
   // it): the CTA-scope proxy fence makes them visible to the bulk-copy engine, the
   // barriers inside the block prefix to the other threads
   {
-    const int nb = (BWD ? 3 : 2) * p.depth;
-    if (tid < nb) {
-      const int k = tid / p.depth, i = tid % p.depth;
-      if (k == 0) mbar_init(&full[i], 1);
-      else if (k == 1) mbar_init(&empty[i], BWD ? 1 : kThreads);  // backward: store warp
-      else mbar_init(&done[i], kThreads);
+    const int nb = (BWD ? 4 : 3) * p.depth;
+    for (int t = tid; t < nb; t += blockDim.x) {
+      const int k = t / p.depth;
+      if (k < 2) mbar_init(&full[t], 1);
+      else if (k == 2) mbar_init(&empty[t - 2 * p.depth], BWD ? 1 : kThreads);  // bwd: store warp
+      else mbar_init(&done[t - 3 * p.depth], kThreads);
       fence_proxy_async_smem();
     }
-    if (tid == 0) s_abort = 0;
-    if (tid < p.depth) slot_row[tid] = -1;
+    if (tid == 0) {
+      s_abort = 0;
+      s_issued = -1;
+    }
   }
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
@@ -136,7 +143,23 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
   const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
   const int nrows = o1 - o0;
-
+  // test hook: the first CTA's producer skips this row's copies (the stage never fills)
+  const int withheld = (blockIdx.x == 0 && blockIdx.y == 0) ? p.withhold_row : -1;
+  // Waits until the copies of the rows before jn have landed (the slots of rows before
+  // jn - depth were handed back, so those have).
+  auto drain = [&](const int jn) {
+    for (int k = max(0, jn - p.depth); k < jn; ++k)
+      if (k != withheld)
+        mbar_wait_bounded(&full[k % (2 * p.depth)],
+                          static_cast<uint32_t>((k / (2 * p.depth)) & 1), kWaitCycles);
+  };
+  // A wait ran out: stop the pipeline, then wait for the producer's copies if it is done
+  // (if not, it sees the stop and waits for them itself; producer_sees_stop).
+  auto stop_and_drain = [&]() {
+    stop_pipeline(&s_abort, p.dev_error);
+    const int jn = read_issued(&s_issued);
+    if (jn >= 0) drain(jn);
+  };
 
   if (tid >= NCT) {
     if constexpr (BWD) {
@@ -172,10 +195,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
           }
         }
         bulk_wait_all();
-        if (bad) {
-          s_abort = 1;
-          if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
-        }
+        if (bad) stop_and_drain();
       }
     }
     if (BWD && tid >= NCT + 64) {
@@ -214,14 +234,14 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     // ------------------------------ producer ------------------------------------------
     if (tid == NCT) {
       const uint64_t pol = l2_evict_first_policy();
-      const int withheld = (blockIdx.x == 0 && blockIdx.y == 0) ? p.withhold_row : -1;
       int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
       int j = 0;
-      int slot = 0;     // j % depth
-      uint32_t ph = 0;  // (j / depth) & 1
-      for (; j < nrows; ++j, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
-        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u, p.wait_cycles)) {
-          s_abort = 1;
+      int slot = 0;      // j % depth
+      uint32_t lap = 0;  // (j / depth) % 4: full barrier slot + (lap & 1) depth, parity lap >> 1
+      for (; j < nrows;
+           ++j, slot = slot + 1 == p.depth ? 0 : slot + 1, lap = (lap + (slot == 0)) & 3u) {
+        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], (lap & 1u) ^ 1u, p.wait_cycles)) {
+          stop_pipeline(&s_abort, p.dev_error);
           break;
         }
         if (*reinterpret_cast<volatile int*>(&s_abort)) break;
@@ -232,32 +252,26 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         const int base = sCu[s] + b * r;
         const bool has_prev = two && b >= 1;
         unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
-        st_release_shared(&slot_row[slot], j);  // the slot's barrier is now in row j's phase
+        uint64_t* fb = &full[slot + ((lap & 1u) ? p.depth : 0)];
         const int boxes = has_prev ? 2 : 1;
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(boxes * r * 128 * 2 +
-                                                                 (BWD ? kLongSlice * 2 : 0)));
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(boxes * r * 128 * 2 +
+                                                        (BWD ? kLongSlice * 2 : 0)));
         if (has_prev) {  // previous block, first-half columns -> tile rows [0, r)
-          tma_load_2d(st, &tm_kv, col0, base - r, &full[slot], pol);
-          tma_load_2d(st + kTile, &tm_sc, col0, base - r, &full[slot], pol);
+          tma_load_2d(st, &tm_kv, col0, base - r, fb, pol);
+          tma_load_2d(st + kTile, &tm_sc, col0, base - r, fb, pol);
         }
         // own block -> tile rows [r, 2r) at coff=2 (second-half columns), [0, r) at coff=1
         const int yo = two ? r * 128 : 0;
         const int x = (two ? d : 0) + col0;
-        tma_load_2d(st + yo, &tm_kv, x, base, &full[slot], pol);
-        tma_load_2d(st + kTile + yo, &tm_sc, x, base, &full[slot], pol);
+        tma_load_2d(st + yo, &tm_kv, x, base, fb, pol);
+        tma_load_2d(st + kTile + yo, &tm_sc, x, base, fb, pol);
         if constexpr (BWD)
           bulk_load_hint(gring + slot * kLongSlice * 2,
-                         p.dout + static_cast<int64_t>(o) * d + col0, kLongSlice * 2,
-                         &full[slot], pol);
+                         p.dout + static_cast<int64_t>(o) * d + col0, kLongSlice * 2, fb, pol);
       }
-      if ((j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) && p.dev_error != nullptr)
-        *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;  // stopped early
-      // Every copy issued here lands before the CTA can exit (consumers that stop early
-      // do not wait for them; slots of rows before j - depth were handed back, so landed).
-      for (int k = max(0, j - p.depth); k < j; ++k)
-        if (k != withheld)
-          mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1),
-                            kWaitCycles);
+      // done: on the normal path the consumers wait for every copy issued here; after a
+      // stop the producer waits for them, unless a stopping thread has seen them
+      if (producer_sees_stop(&s_issued, j, &s_abort)) drain(j);
     }
     return;
   }
@@ -323,23 +337,22 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   // the tile row only through its low three bits, which are those of pg
   const int sw0 = swz(pg, wi) + ch * 8;
   int s = nrows > grp ? find_segment(sB, p.S, o0 + grp) : 0;
-  // stage of row j and its phase parity, advanced by NG rows per iteration (NG < depth):
-  // the new slot is below NG exactly when it wrapped
+  // stage of row j and its lap (j / depth) % 4, advanced by NG rows per iteration (NG <
+  // depth): the new slot is below NG exactly when it wrapped
   int slot = grp;
-  uint32_t ph = 0;
-  for (int j = grp; j < nrows;
-       j += NG, slot = slot + NG >= p.depth ? slot + NG - p.depth : slot + NG, ph ^= slot < NG) {
+  uint32_t lap = 0;
+  for (int j = grp; j < nrows; j += NG,
+           slot = slot + NG >= p.depth ? slot + NG - p.depth : slot + NG,
+           lap = (lap + (slot < NG)) & 3u) {
     const int o = o0 + j;
     s = advance_segment(sB, s, o);
     const int b = o - sB[s];
     const int base = sCu[s] + b * r;
     const bool has_prev = two && b >= 1;
-    // row j's phase of its slot (see wait_shared_eq), then that phase's completion
-    const bool ok = wait_shared_eq(&slot_row[slot], j, p.wait_cycles) &&
-                    mbar_wait_bounded(&full[slot], ph, p.wait_cycles);
+    const bool ok =
+        mbar_wait_bounded(&full[slot + ((lap & 1u) ? p.depth : 0)], lap >> 1, p.wait_cycles);
     if (!__all_sync(0xFFFFFFFFu, ok)) {  // a copy wait ran out: stop, and say so
-      s_abort = 1;
-      if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
+      stop_and_drain();
       break;
     }
     if (__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s_abort) != 0)) break;

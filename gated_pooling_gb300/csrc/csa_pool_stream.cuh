@@ -9,15 +9,15 @@
 // contiguous range of R*C bf16 values. Producer warps stream, for each row of the range,
 // that block of kv and of score (and, backward, the dout row) into a ring of
 // shared-memory stages with 1-D bulk asynchronous copies (TMA), completing on the
-// stage's `full` mbarrier; rows are dealt round robin to the producer warps, since one
-// warp issues about one bulk copy per quarter microsecond. The window of row o is the left half of stage o-1
-// (previous block, coff=2) and the right half of stage o (own block; the whole stage at
-// coff=1), so every consumed byte crosses HBM once. A stage is released (`empty`
-// mbarrier) once rows o and o+1 have read it; ring slots and phases are running counters.
-// The block before o0 (read by row o0 when it is not a segment's first block) is fetched
-// once, left half only, into a buffer laid out like a stage, its row copies issued by the
-// producer warp's lanes together. The mbarriers are set up, one per thread, before the
-// index map is read.
+// row's `full` mbarrier. For small stages the rows are dealt round robin to several
+// producer warps, since one warp issues about one bulk copy per quarter microsecond. The window of
+// row o is the left half of stage o-1 (previous block, coff=2) and the right half of
+// stage o (own block; the whole stage at coff=1), so every consumed byte crosses HBM
+// once. A stage is released (`empty` mbarrier) once rows o and o+1 have read it; ring
+// slots and phases are running counters. The block before o0 (read by row o0 when it is
+// not a segment's first block) is fetched once, left half only, into a buffer laid out
+// like a stage, its row copies issued by producer warp 0's lanes together. The mbarriers
+// are set up before the index map is read.
 //
 // Consumers (NC threads): a thread owns one chunk of VEC columns of a row, the same
 // chunk in both halves; NC/(d/VEC) rows are computed at once (row j -> row slot j mod
@@ -33,11 +33,13 @@
 
 namespace csa {
 
-template <int VEC, int NC, int R, int COFF, bool BWD>
-__global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 0),
+// NP: producer warps (1 for large stages, stream_producers(BWD) for small ones; the block
+// has exactly NP of them, so that a one-producer launch keeps the registers and code of a
+// one-producer block).
+template <int VEC, int NC, int R, int COFF, bool BWD, int NP>
+__global__ void __launch_bounds__(NC + 32 * NP + (BWD ? 32 : 0),
                                   BWD ? CSA_STREAM_BWD_CTAS : CSA_STREAM_FWD_CTAS)
     pool_stream_kernel(const PoolParams p) {
-  constexpr int NP = stream_producers(BWD);  // producer warps
   constexpr int NW = VEC / 2;               // 32-bit words (= column pairs) per chunk
   // ape values per shared-memory vector: pairs in the forward (two 8-byte reads per
   // position measured slightly faster than one 16-byte read), quads in the backward
@@ -48,15 +50,30 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   __shared__ int s_abort;
+  __shared__ int s_issued[NP];  // a finished producer warp's next row (-1: not finished)
   int* sB = reinterpret_cast<int*>(smem);                     // block prefix [S+1]
   int* sCu = sB + p.sB_words;                                  // cu_seqlens [S+1]
   const float* sA = reinterpret_cast<const float*>(smem + p.ape_off);  // [W][NA][V] x AW
   unsigned char* pre = smem + p.pre_off;  // block before the first row: kv, score [R][C]
   unsigned char* stages = smem + p.ring_off;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-  uint64_t* empty = full + p.depth;
+  // Row j's stage is slot j mod depth, released on empty[j mod depth]; its `full` barrier
+  // is full[j mod K depth], K = NP + 1 sets of depth barriers. A phase-parity wait cannot
+  // tell a barrier's phase from the one two phases back, so the barrier's previous row,
+  // j - K depth, must have landed whenever a consumer waits for row j. It has: the
+  // consumer finished row j - NP slots, a row of the same producer warp (NP slots is a
+  // multiple of NP), so that warp had armed its rows up to there, among them row
+  // j - NP depth, and before arming that row it waited until the consumers had handed
+  // back row j - K depth, which they do only after it landed. The same holds for the
+  // previous stage's barrier, row j - 1 (row j - NP slots read stage j - NP slots - 1, or,
+  // as a segment's first block, waited for its arming before releasing it). One producer
+  // arms in order, and K = 2 follows the same way.
+  constexpr int K = NP + 1;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);  // [K depth]
+  uint64_t* empty = full + K * p.depth;                             // [depth]
   uint64_t* pre_bar = empty + p.depth;
-  int* slot_row = reinterpret_cast<int*>(pre_bar + 1);  // row each slot is armed for
+  // several producer warps: the row each slot was last armed for (a segment's first block
+  // waits for its previous row's arming before releasing that stage)
+  int* slot_row = reinterpret_cast<int*>(pre_bar + 1);
 
   const int tid = threadIdx.x;
   const int d = p.d, C = p.C, V = p.V;
@@ -74,14 +91,15 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
   // mbarriers, one per thread, before the map is read: their set-up does not depend on it.
   // The CTA-scope proxy fence makes them visible to the bulk-copy engine; the barriers
   // inside the block prefix make them visible to the other threads.
-  if (tid < 2 * p.depth + 1) {
-    if (tid < p.depth) mbar_init(&full[tid], 1);
-    else if (tid < 2 * p.depth) mbar_init(&empty[tid - p.depth], COFF * V);
+  for (int i = tid; i < (K + 1) * p.depth + 1; i += blockDim.x) {
+    if (i < K * p.depth) mbar_init(&full[i], 1);
+    else if (i < (K + 1) * p.depth) mbar_init(&empty[i - K * p.depth], COFF * V);
     else mbar_init(pre_bar, 1);
     fence_proxy_async_smem();
   }
-  if (tid < p.depth) slot_row[tid] = -1;
+  if (NP > 1 && tid < p.depth) slot_row[tid] = -1;
   if (tid == 0) s_abort = 0;
+  if (tid < NP) s_issued[tid] = -1;
 
   // (the block prefix ends with a barrier: the mbarriers are ready after it)
   const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
@@ -104,6 +122,35 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
     need_pre = o0 > sB[s];
   }
 
+  // test hook: the first CTA's producer skips this row's copies (the stage never fills)
+  const int withheld = (blockIdx.x == 0 && blockIdx.y == 0) ? p.withhold_row : -1;
+  // Waits until the copies that producer warp q issued before its row jn have landed (the
+  // slots of its rows before jn - depth were handed back, so those have), and, for warp
+  // 0, the previous block's copies.
+  auto drain = [&](const int q, const int jn) {
+    for (int k = jn - NP; k >= 0 && k >= jn - p.depth; k -= NP)
+      if (k != withheld)
+        mbar_wait_bounded(&full[k % (K * p.depth)],
+                          static_cast<uint32_t>((k / (K * p.depth)) & 1), kWaitCycles);
+    if (q == 0 && need_pre) mbar_wait_bounded(pre_bar, 0, kWaitCycles);
+  };
+  // A wait ran out: stop the pipeline, then wait for the copies of the producer warps that
+  // are done (the others see the stop and wait for their own; producer_sees_stop).
+  auto stop_and_drain = [&]() {
+    stop_pipeline(&s_abort, p.dev_error);
+    for (int q = 0; q < NP; ++q) {
+      const int jn = read_issued(&s_issued[q]);
+      if (jn >= 0) drain(q, jn);
+    }
+  };
+
+  // row j's full barrier and phase parity from its slot and lap = (j / depth) mod 2K
+  auto fbar = [&](const int slot, const uint32_t lap) {
+    return &full[slot + static_cast<int>(lap >= K ? lap - K : lap) * p.depth];
+  };
+  auto fpar = [](const uint32_t lap) { return lap >= K ? 1u : 0u; };
+  auto next_lap = [](const uint32_t lap) { return lap + 1 == 2 * K ? 0u : lap + 1; };
+
   uint64_t acc[W][NW];  // backward: dAPE sums, column pairs
 #pragma unroll
   for (int i = 0; i < W; ++i)
@@ -115,8 +162,10 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
     // NP producer warps; lane 0 of warp pw streams the rows j = pw, pw + NP, ... into ring
     // slots j mod depth (depth is a multiple of NP, so every slot has one producer). A warp
     // has one bulk copy in issue at a time (about a quarter of a microsecond each on GB300),
-    // so several warps issuing side by side keep the copy engine busy. Warp 0's lanes first
-    // issue the previous block's 2*R row copies together. (Warp NP: the backward's zero warp.)
+    // so for small stages several warps issue side by side; large stages keep the copy
+    // engine busy from one warp, and the plan uses one.
+    // Warp 0's lanes first issue the previous block's 2*R row copies together. (Warp NP:
+    // the backward's zero warp.)
     const int pw = (tid - NC) >> 5;
     const int lane = (tid - NC) & 31;
     const uint64_t pol = l2_evict_first_policy();
@@ -153,47 +202,41 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
       if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, V, lane, 32);
     }
     if (pw < NP && lane == 0) {
-      const int withheld = (blockIdx.x == 0 && blockIdx.y == 0) ? p.withhold_row : -1;
       int s = nrows > pw ? find_segment(sB, p.S, o0 + pw) : 0;
       int j = pw;
       int slot = pw;     // j % depth
-      uint32_t ph = 0;   // (j / depth) & 1
+      uint32_t lap = 0;  // (j / depth) mod 2K
       for (; j < nrows; j += NP) {
-        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], ph ^ 1u, p.wait_cycles)) {
-          s_abort = 1;
+        // the slot's previous row, j - depth, has been handed back (its `empty` phase)
+        // ((j / depth) - 1) & 1 = (lap & 1) ^ 1, 2K being even
+        if (j >= p.depth && !mbar_wait_bounded(&empty[slot], (lap & 1u) ^ 1u, p.wait_cycles)) {
+          stop_and_drain();
           break;
         }
         if (*reinterpret_cast<volatile int*>(&s_abort)) break;
         const int o = o0 + j;
         s = advance_segment(sB, s, o);
+        uint64_t* fb = fbar(slot, lap);
+        if constexpr (NP > 1) st_release_shared(&slot_row[slot], j);
         if (j != withheld) {  // test hook: a withheld stage never fills
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(stage_g + (BWD ? d * 2 : 0)));
           const int base = sCu[s] + (o - sB[s]) * R;
           unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
-          st_release_shared(&slot_row[slot], j);  // the slot's barrier is now in row j's phase
-          mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_g + (BWD ? d * 2 : 0)));
           const int64_t off = static_cast<int64_t>(base) * C;
-          bulk_load_hint(st, p.kv + off, kv_bytes, &full[slot], pol);
-          bulk_load_hint(st + kv_bytes, p.score + off, kv_bytes, &full[slot], pol);
+          bulk_load_hint(st, p.kv + off, kv_bytes, fb, pol);
+          bulk_load_hint(st + kv_bytes, p.score + off, kv_bytes, fb, pol);
           if constexpr (BWD)
-            bulk_load_hint(st + stage_g, p.dout + static_cast<int64_t>(o) * d, d * 2, &full[slot],
-                           pol);
+            bulk_load_hint(st + stage_g, p.dout + static_cast<int64_t>(o) * d, d * 2, fb, pol);
         }
         slot += NP;
         if (slot >= p.depth) {
           slot -= p.depth;
-          ph ^= 1u;
+          lap = next_lap(lap);
         }
       }
-      if ((j < nrows || *reinterpret_cast<volatile int*>(&s_abort)) && p.dev_error != nullptr)
-        *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;  // stopped early
-      // Every copy this warp issued lands before the CTA can exit: normally the consumers
-      // have waited for all of them already, but consumers that stop early have not. (The
-      // slots of this warp's rows before j - depth were handed back, so those landed.)
-      for (int k = j - NP; k >= 0 && k >= j - p.depth; k -= NP)
-        if (k != withheld)
-          mbar_wait_bounded(&full[k % p.depth], static_cast<uint32_t>((k / p.depth) & 1),
-                            kWaitCycles);
-      if (pw == 0 && need_pre) mbar_wait_bounded(pre_bar, 0, kWaitCycles);
+      // done: on the normal path the consumers wait for every copy issued here; after a
+      // stop this warp waits for its own, unless a stopping thread has seen them
+      if (producer_sees_stop(&s_issued[pw], j, &s_abort)) drain(pw, j);
     }
   } else {
     // ------------------------------ consumers -----------------------------------------
@@ -223,10 +266,10 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
       // stage of row j and its phase parity, advanced by `slots` rows per iteration
       // (slots < depth), and the same for row j - 1
       int slot = rs;  // rs < slots < depth
-      uint32_t ph = 0;
+      uint32_t lap = 0;  // (j / depth) mod 2K, as the producers count it
       for (int j = rs; j < nrows; j += p.slots) {
         const int pslot = slot == 0 ? p.depth - 1 : slot - 1;
-        const uint32_t pph = slot == 0 ? ph ^ 1u : ph;
+        const uint32_t plap = slot != 0 ? lap : lap == 0 ? 2 * K - 1 : lap - 1;
         const int o = o0 + j;
         s = advance_segment(sB, s, o);
         const int b = o - sB[s];
@@ -234,9 +277,7 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
         const int cs = sCu[s];
         const int base = cs + b * R;
         const bool has_prev = TWO && b >= 1;
-        // row j's phase of its slot (see wait_shared_eq), then that phase's completion
-        bool ok = wait_shared_eq(&slot_row[slot], j, p.wait_cycles) &&
-                  mbar_wait_bounded(&full[slot], ph, p.wait_cycles);
+        bool ok = mbar_wait_bounded(fbar(slot, lap), fpar(lap), p.wait_cycles);
         // kv chunk of the own block's first token; score sits kv_bytes further, rows are C2
         // bytes apart. The previous block (coff=2) uses the same layout (its own stage, or
         // the block fetched before the first row).
@@ -249,14 +290,12 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
             ok = ok && mbar_wait_bounded(pre_bar, 0, p.wait_cycles);
             prev_kv = pre + c0 * 2;
           } else {
-            ok = ok && wait_shared_eq(&slot_row[pslot], j - 1, p.wait_cycles) &&
-                 mbar_wait_bounded(&full[pslot], pph, p.wait_cycles);
+            ok = ok && mbar_wait_bounded(fbar(pslot, plap), fpar(plap), p.wait_cycles);
             prev_kv = stages + static_cast<size_t>(pslot) * p.stage_bytes + c0 * 2;
           }
         }
         if (!ok) {  // a copy wait ran out: stop, and say so
-          s_abort = 1;
-          if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
+          stop_and_drain();
           break;
         }
         if (*reinterpret_cast<volatile int*>(&s_abort)) break;
@@ -414,15 +453,15 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
           }
         }
         // release the own stage and (coff=2) the previous one, which row o-1 also read. A
-        // segment's first block has not read the previous stage and so has not seen it
-        // armed for row j-1: with several producer warps row j can be armed before row j-1,
-        // and an arrival on the previous slot's `empty` barrier before that would count
-        // toward the slot's earlier phase. So it waits for row j-1's arming first.
+        // segment's first block has not read the previous stage; its arrival there counts
+        // toward row j - 1's phase only once row j - 1 is armed (its producer waited for
+        // that slot's earlier phase). One producer arms in order, so row j armed means row
+        // j - 1 armed; with several, the first block waits for row j - 1's arming.
         mbar_arrive(&empty[slot]);
         if (TWO && j >= 1) {
-          if (!has_prev && !wait_shared_eq(&slot_row[pslot], j - 1, p.wait_cycles)) {
-            s_abort = 1;
-            if (p.dev_error != nullptr) *reinterpret_cast<volatile int32_t*>(p.dev_error) = 3;
+          if (NP > 1 && !has_prev && !wait_shared_eq(&slot_row[pslot], j - 1, &s_abort,
+                                                    p.wait_cycles)) {
+            stop_and_drain();
             break;
           }
           mbar_arrive(&empty[pslot]);
@@ -430,7 +469,7 @@ __global__ void __launch_bounds__(NC + 32 * stream_producers(BWD) + (BWD ? 32 : 
         slot += p.slots;
         if (slot >= p.depth) {
           slot -= p.depth;
-          ph ^= 1u;
+          lap = next_lap(lap);
         }
       }
     }

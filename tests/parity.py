@@ -10,9 +10,11 @@ out, dKV, dScore (bf16): an element passes if
       exponent arguments, see oracle/csa_oracle.cpp), u32 = 2^-24.
 dAPE (fp32): |gpu - ref| <= 1e-5 |ref| + KAPPA * u32 * err_dape.
 ulp(y) is the bf16 spacing at |y| (2^(e-8) for |y| in [2^(e-1), 2^e)), and the
-subnormal spacing 2^-133 at zero. KAPPA = 32 bounds the constants of that analysis
-for windows up to a few hundred positions (fp32 exponent and summation errors).
-The report counts how many elements needed clause (2); the tests cap that count.
+subnormal spacing 2^-133 at zero. KAPPA = 8: a plain float32 evaluation of every window
+stays within 8 u32 x mass (pinned on the CPU for windows of 4..256 positions), and the
+CUDA kernels used at most 5.3 on every parity pack (the per-pack record is kept with the
+profiles). The report counts how many elements needed clause (2) and the largest kappa
+one of them used; the tests cap the count.
 """
 import dataclasses
 
@@ -21,7 +23,7 @@ import numpy as np
 import thd_synth as ts
 
 U32 = 2.0 ** -24
-KAPPA = 32.0
+KAPPA = 8.0
 
 
 def bits_to_f64(bits):
@@ -43,10 +45,11 @@ class Report:
     clause2: int
     fail: int
     worst: list
+    kappa_used: float = 0.0  # largest kappa an element needing clause 2 required
 
     def __str__(self):
         return (f"{self.name}: n={self.n} bit-exact={self.exact} needed-clause2={self.clause2} "
-                f"fail={self.fail} worst={self.worst[:3]}")
+                f"kappa-used={self.kappa_used:.2f} fail={self.fail} worst={self.worst[:3]}")
 
 
 def compare_bf16(name, gpu_bits, ref_bits, ref_f64=None, err=None, kappa=KAPPA):
@@ -59,27 +62,36 @@ def compare_bf16(name, gpu_bits, ref_bits, ref_f64=None, err=None, kappa=KAPPA):
     ok1 &= ~np.isnan(g)
     ok = ok1.copy()
     need2 = np.zeros_like(ok)
+    kappa_used = 0.0
     if ref_f64 is not None and err is not None:
         ref = np.asarray(ref_f64).reshape(-1)
         e = np.asarray(err).reshape(-1)
         bad = ~ok1
         if bad.any():
-            tol = ulp_bf16(ref[bad]) + kappa * U32 * e[bad]
-            ok2 = np.abs(g[bad] - ref[bad]) <= tol
+            dev = np.abs(g[bad] - ref[bad]) - ulp_bf16(ref[bad])
+            tol = kappa * U32 * e[bad]
+            ok2 = dev <= tol
             ok[bad] = ok2
             need2[np.flatnonzero(bad)[ok2]] = True
+            if ok2.any():
+                kappa_used = float(np.max(np.maximum(dev[ok2], 0) / (U32 * e[bad][ok2] + 1e-300)))
     idx = np.flatnonzero(~ok)
     worst = [(int(i), float(g[i]), float(rb[i])) for i in idx[:5]]
-    return Report(name, int(g.size), int(exact.sum()), int(need2.sum()), int(idx.size), worst)
+    return Report(name, int(g.size), int(exact.sum()), int(need2.sum()), int(idx.size), worst,
+                  kappa_used)
 
 
 def compare_dape(gpu, ref_f64, err, kappa=KAPPA, rel=1e-5):
     gpu = np.asarray(gpu, dtype=np.float64).reshape(-1)
     ref = np.asarray(ref_f64).reshape(-1)
-    tol = rel * np.abs(ref) + kappa * U32 * np.asarray(err).reshape(-1)
-    ok = np.abs(gpu - ref) <= tol
-    rel_ok = np.abs(gpu - ref) <= rel * np.abs(ref)
+    e = np.asarray(err).reshape(-1)
+    dev = np.abs(gpu - ref) - rel * np.abs(ref)
+    tol = kappa * U32 * e
+    ok = dev <= tol
+    rel_ok = dev <= 0
     idx = np.flatnonzero(~ok)
     worst = [(int(i), float(gpu[i]), float(ref[i])) for i in idx[:5]]
-    return Report("dape", int(gpu.size), int(rel_ok.sum()), int((ok & ~rel_ok).sum()),
-                  int(idx.size), worst)
+    used = ok & ~rel_ok
+    kappa_used = float(np.max(dev[used] / (U32 * e[used] + 1e-300))) if used.any() else 0.0
+    return Report("dape", int(gpu.size), int(rel_ok.sum()), int(used.sum()), int(idx.size), worst,
+                  kappa_used)

@@ -23,7 +23,10 @@ from tests.parity import compare_bf16, compare_dape
 
 pytestmark = pytest.mark.gpu
 
-CLAUSE2_CAP = 2e-4  # fraction of elements allowed to need the cancellation clause
+# Fraction of a tensor's elements allowed to need the cancellation clause (at least 2
+# elements): the largest fraction seen on any parity pack times about 2.5 (out 7.6e-6 on
+# the long-window pack, dScore 8.1e-5 on the 16384-segment ratio=2 pack, dKV none).
+CLAUSE2_CAP = {"out": 2e-5, "dkv": 1e-6, "dscore": 2e-4}
 
 
 def log_reports(label, *reports):
@@ -35,7 +38,8 @@ def log_reports(label, *reports):
     with open(path, "a") as fh:
         for r in reports:
             fh.write(json.dumps({"case": label, "tensor": r.name, "n": r.n, "exact": r.exact,
-                                 "clause2": r.clause2, "fail": r.fail}) + "\n")
+                                 "clause2": r.clause2, "kappa_used": r.kappa_used,
+                                 "fail": r.fail}) + "\n")
 
 
 def small_packs():
@@ -129,7 +133,7 @@ def check_fwd(gp, pack, shift=0, label=None):
     print(pack.name, rep)
     log_reports(label or pack.name, rep)
     assert rep.fail == 0, str(rep)
-    assert rep.clause2 <= max(2, CLAUSE2_CAP * rep.n), str(rep)
+    assert rep.clause2 <= max(2, CLAUSE2_CAP["out"] * rep.n), str(rep)
     return rep
 
 
@@ -145,7 +149,7 @@ def check_bwd(gp, pack, shift=0, label=None):
     for rep in (r1, r2, r3):
         assert rep.fail == 0, str(rep)
     for rep in (r1, r2):
-        assert rep.clause2 <= max(2, CLAUSE2_CAP * rep.n), str(rep)
+        assert rep.clause2 <= max(2, CLAUSE2_CAP[rep.name] * rep.n), str(rep)
     # never-consumed slots are exact +0
     zero = ref["owners"] == 0
     assert (dkv.reshape(ref["owners"].shape)[zero] == 0).all()

@@ -428,6 +428,8 @@ MASS_PACKS = {
                                        score_scale=4.0),
     "r128c1_x4": lambda: ts.make_custom([512, 300], ratio=128, coff=1, d=16, seed=5,
                                         score_scale=4.0),
+    "r128c2_x4": lambda: ts.make_custom([600, 256], ratio=128, coff=2, d=8, seed=6,
+                                        score_scale=4.0),
 }
 KAPPA_F32 = 8.0  # a plain float32 evaluation stays within KAPPA_F32 * u32 * mass
 
@@ -435,7 +437,7 @@ KAPPA_F32 = 8.0  # a plain float32 evaluation stays within KAPPA_F32 * u32 * mas
 @pytest.mark.parametrize("name", sorted(MASS_PACKS))
 def test_fp32_evaluation_within_error_masses(oracle_lib, name):
     """The masses are large enough: a plain float32 evaluation of every window (windows of
-    4 to 128 positions, sharpened scores included) differs from the fp64 result by at most
+    4 to 256 positions, sharpened scores included) differs from the fp64 result by at most
     KAPPA_F32 * u32 * mass, element by element, for out, dKV, dScore and dAPE. (A mass that
     drops a term, e.g. the exponent-argument factor, fails here on the long windows.)"""
     pack = MASS_PACKS[name]()
