@@ -24,9 +24,10 @@ from tests.parity import compare_bf16, compare_dape
 pytestmark = pytest.mark.gpu
 
 # Fraction of a tensor's elements allowed to need the cancellation clause (at least 2
-# elements): the largest fraction seen on any parity pack times about 2.5 (out 7.6e-6 on
-# the long-window pack, dScore 8.1e-5 on the 16384-segment ratio=2 pack, dKV none).
-CLAUSE2_CAP = {"out": 2e-5, "dkv": 1e-6, "dscore": 2e-4}
+# elements), from the largest fraction seen on any parity pack: out 7.6e-6 on the
+# long-window pack (cap 2e-5), dScore 8.1e-5 on the 16384-segment ratio=2 pack (cap 1e-4),
+# dKV none (cap 1e-6).
+CLAUSE2_CAP = {"out": 2e-5, "dkv": 1e-6, "dscore": 1e-4}
 
 
 def log_reports(label, *reports):
