@@ -21,7 +21,7 @@ _LIB_PATH = os.path.join(_HERE, "libcsa_oracle.so")
 _lib: Optional[ctypes.CDLL] = None
 
 ERRORS = {0: "ok", 1: "bad arguments", 2: "invalid cu_seqlens", 3: "out_rows < total_comp",
-          4: "a slot was read by two window positions"}
+          4: "a slot was read by two window positions", 5: "negative lead"}
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
@@ -66,6 +66,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_oracle_hardware_threads.argtypes = []
     lib.csa_oracle_round_bf16.restype = None
     lib.csa_oracle_round_bf16.argtypes = [vp, i64, vp]
+    lib.csa_oracle_kpool_total.restype = i64
+    lib.csa_oracle_kpool_total.argtypes = [vp, vp, i32, i32]
+    lib.csa_oracle_kpool_fwd.restype = i32
+    lib.csa_oracle_kpool_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, vp, vp, vp,
+                                         vp, i32]
     if path is None:
         _lib = lib
     return lib
@@ -213,3 +218,49 @@ def fwd_pack(pack, **kw):
 def bwd_pack(pack, **kw):
     return bwd(pack.kv, pack.score, pack.ape, pack.cu_seqlens, pack.dout, pack.ratio, pack.coff,
                pack.d, pack.capacity, **kw)
+
+
+# ----------------------------------------------------------------------------------
+# KPool (the DSA indexer's key pooling)
+# ----------------------------------------------------------------------------------
+
+def kpool_total(cu_seqlens, lead, pool: int, lib: Optional[ctypes.CDLL] = None) -> int:
+    """Number of pools: sum over segments of floor((seqlen - lead) / pool)."""
+    lib = lib or load()
+    cu = _c(cu_seqlens, np.int32)
+    ld = None if lead is None else _c(lead, np.int32)
+    n = lib.csa_oracle_kpool_total(_p(cu), _p(ld), cu.shape[0] - 1, pool)
+    if n < 0:
+        raise OracleError("kpool_total: bad arguments")
+    return int(n)
+
+
+def kpool_fwd(key, gate, cu_seqlens, lead, pool: int, d: int, capacity: int,
+              out_rows: Optional[int] = None, *, compress: bool = False, want_f64: bool = False,
+              want_err: bool = False, nthreads: int = 1,
+              lib: Optional[ctypes.CDLL] = None) -> Dict[str, np.ndarray]:
+    """KPool forward. Returns {"out": uint16 [out_rows, d], optional "out_f64", "out_err"
+    and "out_slack" (the last two with want_err)}."""
+    lib = lib or load()
+    cu = _c(cu_seqlens, np.int32)
+    ld = None if lead is None else _c(lead, np.int32)
+    if out_rows is None:
+        out_rows = kpool_total(cu, ld, pool, lib)
+    key, gate = _c(key, np.uint16), _c(gate, np.uint16)
+    res = {"out": np.zeros((out_rows, d), dtype=np.uint16)}
+    if want_f64:
+        res["out_f64"] = np.zeros((out_rows, d), dtype=np.float64)
+    if want_err:
+        res["out_err"] = np.zeros((out_rows, d), dtype=np.float64)
+        res["out_slack"] = np.zeros((out_rows, d), dtype=np.float64)
+    _check(lib.csa_oracle_kpool_fwd(_p(key), _p(gate), _p(cu), _p(ld), cu.shape[0] - 1, pool, d,
+                                    capacity, out_rows, 1 if compress else 0, _p(res["out"]),
+                                    _p(res.get("out_f64")), _p(res.get("out_err")),
+                                    _p(res.get("out_slack")), max(1, nthreads)), "kpool_fwd")
+    return res
+
+
+def kpool_fwd_pack(pack, **kw):
+    return kpool_fwd(pack.key, pack.gate, pack.cu_seqlens, pack.lead, pack.pool, pack.d,
+                     pack.capacity, **kw)
+

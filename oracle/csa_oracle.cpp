@@ -80,7 +80,7 @@ uint16_t double_to_bf16_bits(double x) {
 
 // Error codes shared by every entry point of the oracle.
 enum { ORACLE_OK = 0, ORACLE_BAD_ARGS = 1, ORACLE_BAD_CU = 2, ORACLE_OUT_ROWS = 3,
-       ORACLE_DOUBLE_WRITE = 4 };
+       ORACLE_DOUBLE_WRITE = 4, ORACLE_BAD_LEAD = 5 };
 
 int check_args(const int32_t* cu, int S, int ratio, int coff, int d, int64_t capacity) {
   if (cu == nullptr || S < 0 || ratio < 1 || (coff != 1 && coff != 2) || d < 1 ||
@@ -349,6 +349,150 @@ int bwd_impl(const uint16_t* kv, const uint16_t* score, const float* ape,
   return ORACLE_OK;
 }
 
+// ---------------------------------------------------------------------------------
+// KPool: the DSA indexer's key pooling ("Megatron-LM PR #8835", the KPool commits: the
+// commit that adds "dsa_indexer_kpool_key_dtype_compression" and the explicit-mask pool
+// origin, and the one that squashes the tail-less certificate fix and the empty-query
+// guard; KPool selection itself is NVIDIA#8287 there).
+//
+// Keys of one segment are grouped into pools of P consecutive keys ("pooled keys on the
+// grid [0:4], [4:8], ..."), the grid starting at the segment's first valid key: packed
+// pooling resets at every segment, and the pool origin is the first valid key of each
+// sample. A pool becomes one pooled key: per column, an FP32 softmax of the gate over
+// the pool's keys weights the keys ("FP32 pool softmax").
+//  * default: the weighted sum is taken in FP32 and cast to bf16 once ("the FP32
+//    weighted reduction and BF16 output of the existing KPool implementation");
+//  * key-dtype compression: the FP32 softmax is cast to the key dtype (bf16) before
+//    multiplying and reducing: each weight is rounded to bf16, each weight x key
+//    product to bf16, and their sum is cast to bf16.
+// Keys after the last complete pool of a segment (its incomplete tail) form no pool:
+// tail selection appends those keys individually, which is part of the selection, not
+// of the pooling. Readings where the page is silent:
+//  * the gate has the keys' shape [tokens, d]: one softmax per pool and column (the
+//    gate has a key axis; a per-key gate is the case of equal columns);
+//  * the FP32 softmax weight is the exact weight rounded to fp32; its cast to bf16,
+//    the products and the final cast round to nearest even;
+//  * the sum of the bf16 products is formed exactly (compensated) and rounded once;
+//  * the first valid key of segment s is cu_seqlens[s] + lead[s] (lead >= 0; a lead at
+//    or past the segment's end leaves it without pools).
+
+// The pools in output order: pool o starts at token start[o].
+std::vector<int64_t> list_pools(const int32_t* cu, const int32_t* lead, int S, int P) {
+  std::vector<int64_t> start;
+  for (int s = 0; s < S; ++s) {
+    const int64_t first = static_cast<int64_t>(cu[s]) + (lead != nullptr ? lead[s] : 0);
+    const int64_t valid = static_cast<int64_t>(cu[s + 1]) - first;
+    const int64_t n = valid > 0 ? valid / P : 0;
+    for (int64_t b = 0; b < n; ++b) start.push_back(first + b * P);
+  }
+  return start;
+}
+
+int check_kpool_args(const int32_t* cu, const int32_t* lead, int S, int P, int d,
+                     int64_t capacity) {
+  const int rc = check_args(cu, S, P, 1, d, capacity);
+  if (rc != ORACLE_OK) return rc;
+  if (lead != nullptr)
+    for (int s = 0; s < S; ++s)
+      if (lead[s] < 0) return ORACLE_BAD_LEAD;
+  return ORACLE_OK;
+}
+
+// One pool and column: weights, pooled value in both modes, error mass and slack.
+struct PoolColumn {
+  double o = 0.0;      // the pooled value before its final bf16 cast
+  double err = 0.0;    // first-order fp32 error mass (units of the fp32 unit roundoff)
+  double slack = 0.0;  // compression: absolute change a different bf16 weight could make
+};
+
+// Weights of an fp32 evaluation are only close to the exact ones: the half-width of the
+// interval an fp32 weight can land in, in units of the fp32 unit roundoff, is taken as
+// 8 x p x (P + 6 + 2(|x_i| + |m|) + 2 max_j(|x_j| + |m|)): the exponent argument's
+// absolute error (~ |x| + |m|, in the exponent of each term and of the normaliser), the
+// exponential's and the reciprocal's roundings and the P-term normaliser sum. Where that
+// interval holds a bf16 rounding boundary, the compressed weight is not decided by the
+// arithmetic, and the slack is the largest change the other choice makes to the pooled
+// value (pins in tests/test_kpool_oracle.py).
+PoolColumn pool_column(const uint16_t* key, const uint16_t* gate, int64_t start, int P, int d,
+                       int64_t j, bool compress) {
+  std::vector<double> x(P), v(P), p(P);
+  for (int i = 0; i < P; ++i) {
+    const int64_t flat = (start + i) * d + j;
+    x[i] = bf16_bits_to_double(gate[flat]);
+    v[i] = bf16_bits_to_double(key[flat]);
+  }
+  double m = x[0];
+  for (int i = 1; i < P; ++i)
+    if (x[i] > m) m = x[i];
+  double z = 0.0;
+  for (int i = 0; i < P; ++i) {
+    p[i] = std::exp(x[i] - m);
+    z += p[i];
+  }
+  for (int i = 0; i < P; ++i) p[i] /= z;
+  PoolColumn r;
+  if (!compress) {
+    for (int i = 0; i < P; ++i) r.o += p[i] * v[i];
+    for (int i = 0; i < P; ++i)
+      r.err += p[i] * (std::fabs(v[i]) + std::fabs(v[i] - r.o) * (1.0 + std::fabs(x[i]) + std::fabs(m)));
+    return r;
+  }
+  double xspread = 0.0;
+  for (int i = 0; i < P; ++i) xspread = std::max(xspread, std::fabs(x[i]) + std::fabs(m));
+  const double u32 = std::ldexp(1.0, -24);
+  double abs_sum = 0.0;
+  double comp = 0.0;  // Neumaier compensation: the P-term sum of products, exact here
+  for (int i = 0; i < P; ++i) {
+    const double pf = static_cast<double>(static_cast<float>(p[i]));       // FP32 weight
+    const double pb = bf16_bits_to_double(double_to_bf16_bits(pf));         // cast to bf16
+    const double prod = bf16_bits_to_double(double_to_bf16_bits(pb * v[i]));  // bf16 product
+    const double t = r.o + prod;
+    comp += std::fabs(r.o) >= std::fabs(prod) ? (r.o - t) + prod : (prod - t) + r.o;
+    r.o = t;
+    abs_sum += std::fabs(prod);
+    const double half = 8.0 * u32 * p[i] *
+                        (P + 6.0 + 2.0 * (std::fabs(x[i]) + std::fabs(m)) + 2.0 * xspread);
+    // bf16 rounding is monotone: the ends of the interval give the extreme choices
+    double worst = 0.0;
+    for (const double q : {p[i] - half, p[i] + half}) {
+      const double qb =
+          bf16_bits_to_double(double_to_bf16_bits(static_cast<double>(static_cast<float>(q))));
+      const double alt = bf16_bits_to_double(double_to_bf16_bits(qb * v[i]));
+      if (qb != pb) worst = std::max(worst, std::fabs(alt - prod));
+    }
+    r.slack += worst;
+  }
+  r.o += comp;
+  // the kernel adds the P products in fp32: at most (P - 1) roundings of partial sums
+  r.err = P * abs_sum;
+  return r;
+}
+
+int kpool_impl(const uint16_t* key, const uint16_t* gate, const int32_t* cu, const int32_t* lead,
+               int S, int P, int d, int64_t capacity, int64_t out_rows, int compress,
+               uint16_t* out_bf16, double* out_f64, double* out_err, double* out_slack,
+               int nthreads) {
+  int rc = check_kpool_args(cu, lead, S, P, d, capacity);
+  if (rc != ORACLE_OK) return rc;
+  if (compress != 0 && compress != 1) return ORACLE_BAD_ARGS;
+  const std::vector<int64_t> pools = list_pools(cu, lead, S, P);
+  if (static_cast<int64_t>(pools.size()) > out_rows) return ORACLE_OUT_ROWS;
+  if (!pools.empty() && (key == nullptr || gate == nullptr || out_bf16 == nullptr))
+    return ORACLE_BAD_ARGS;
+  over_row_ranges(static_cast<int64_t>(pools.size()), nthreads < 1 ? 1 : nthreads,
+                  [&](int, int64_t o_begin, int64_t o_end) {
+    for (int64_t o = o_begin; o < o_end; ++o)
+      for (int64_t j = 0; j < d; ++j) {
+        const PoolColumn r = pool_column(key, gate, pools[o], P, d, j, compress != 0);
+        out_bf16[o * d + j] = double_to_bf16_bits(r.o);
+        if (out_f64 != nullptr) out_f64[o * d + j] = r.o;
+        if (out_err != nullptr) out_err[o * d + j] = r.err;
+        if (out_slack != nullptr) out_slack[o * d + j] = r.slack;
+      }
+  });
+  return ORACLE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -445,6 +589,30 @@ int csa_oracle_hardware_threads(void) {
 // Round doubles to bf16 bit patterns (exposed so the pins can test the rounding).
 void csa_oracle_round_bf16(const double* x, int64_t n, uint16_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = double_to_bf16_bits(x[i]);
+}
+
+// KPool: number of pools (sum over segments of floor((seqlen - lead) / P), segments
+// whose lead reaches their end contributing none); -1 on bad arguments.
+int64_t csa_oracle_kpool_total(const int32_t* cu_seqlens, const int32_t* lead, int S, int P) {
+  if (cu_seqlens == nullptr || S < 0 || P < 1) return -1;
+  for (int s = 0; s < S; ++s)
+    if (cu_seqlens[s + 1] < cu_seqlens[s] || (lead != nullptr && lead[s] < 0)) return -1;
+  return static_cast<int64_t>(list_pools(cu_seqlens, lead, S, P).size());
+}
+
+// KPool forward. key, gate: bf16 bit patterns [capacity, d]; lead: int32 [S] or NULL
+// (zeros); out_bf16: [out_rows, d] (rows past the pool count are left untouched);
+// compress: 0 = FP32 weighted sum, 1 = key-dtype compression. Optional (may be NULL):
+// out_f64 (value before the final cast), out_err (error mass, units of the fp32 unit
+// roundoff), out_slack (compression: absolute change an undecided bf16 weight could
+// make). nthreads >= 1 host threads over contiguous pool ranges (same results).
+int csa_oracle_kpool_fwd(const uint16_t* key, const uint16_t* gate, const int32_t* cu_seqlens,
+                         const int32_t* lead, int S, int P, int d, int64_t capacity,
+                         int64_t out_rows, int compress, uint16_t* out_bf16, double* out_f64,
+                         double* out_err, double* out_slack, int nthreads) {
+  if (nthreads < 1) return ORACLE_BAD_ARGS;
+  return kpool_impl(key, gate, cu_seqlens, lead, S, P, d, capacity, out_rows, compress,
+                    out_bf16, out_f64, out_err, out_slack, nthreads);
 }
 
 }  // extern "C"

@@ -16,12 +16,17 @@ Generator (counter based, so any slice of any tensor can be reproduced alone):
 * A bf16 value is the round-to-nearest-even of the float32 rounding of the
   float64 normal, stored as its 16-bit pattern (``uint16``).
 * Each tensor has its own stream: key = ``mix64(seed * GOLDEN + tag)`` with tags
-  kv=1, score=2, ape=3, dout=4, lengths=5.
+  kv=1, score=2, ape=3, dout=4, lengths=5, and for the KPool packs key=6, gate=7,
+  lead=8.
 
 The workloads follow the shapes and distributions of the pages' THD packs
 (ratio=4 / coff=2 packs of 8192-token sequences at head dims 128 and 512), plus a
 tiny ragged pack, a ragged ratio=2 pack and a long-window ratio=128 pack. No
 dataset is involved: the pages measure synthetic packs only.
+
+KPool packs (the DSA indexer's key pooling) hold indexer keys and gates [tokens, d]
+(both N(0,1) bf16), THD segments, and optionally each segment's lead (the offset of
+its first valid key, drawn uniformly in [0, max_lead]); the pools are P keys wide.
 """
 from __future__ import annotations
 
@@ -35,6 +40,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 TAG_KV, TAG_SCORE, TAG_APE, TAG_DOUT, TAG_LENGTHS = 1, 2, 3, 4, 5
+TAG_KEY, TAG_GATE, TAG_LEAD = 6, 7, 8
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -215,3 +221,116 @@ def bf16_tensor_bits(t) -> np.ndarray:
     """uint16 bit patterns of a torch bf16 tensor (copied to the host)."""
     import torch
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------------------------
+# KPool packs
+# ----------------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class KPoolPack:
+    """One synthetic KPool input, host side (numpy)."""
+    name: str
+    pool: int
+    d: int
+    capacity: int
+    cu_seqlens: np.ndarray        # int32 [S+1]
+    lead: Optional[np.ndarray]    # int32 [S] (first valid key of segment s: cu[s] + lead[s]) or None
+    key: np.ndarray               # uint16 (bf16 bits) [capacity, d]
+    gate: np.ndarray              # uint16 (bf16 bits) [capacity, d]
+
+    @property
+    def S(self) -> int:
+        return int(self.cu_seqlens.shape[0] - 1)
+
+    @property
+    def total_pools(self) -> int:
+        lens = np.diff(self.cu_seqlens.astype(np.int64))
+        lead = np.zeros_like(lens) if self.lead is None else self.lead.astype(np.int64)
+        return int(np.sum(np.maximum(lens - lead, 0) // self.pool))
+
+
+@dataclasses.dataclass(frozen=True)
+class KPoolSpec:
+    name: str
+    lengths: Optional[List[int]]  # None: drawn like the ragged compressor pack
+    pool: int
+    d: int
+    pad_rows: int = 0
+    max_lead: int = 0             # > 0: leads drawn uniformly in [0, max_lead]
+    leads: Optional[List[int]] = None  # explicit leads (instead of drawn ones)
+    gate_scale: float = 1.0       # exact power-of-two scale applied to bf16 gates
+    seed: int = 0
+    length_seed: int = 7
+    n_drawn_segments: int = 16
+    max_drawn_length: int = 4096
+
+
+# Indexer keys of head dim 128 pooled four at a time (the pages' grid [0:4], [4:8], ...):
+# a tiny ragged pack with leads, a 16-sequence pack of 8192 tokens, a ragged pack with
+# leads and padding, and the 64-sequence bench pack (512k keys, larger than L2).
+KPOOL_SPECS: Dict[str, KPoolSpec] = {
+    "kpool_tiny": KPoolSpec("kpool_tiny", [13, 4, 0, 9, 2, 11], pool=4, d=8, pad_rows=5,
+                            leads=[1, 3, 0, 2, 5, 0]),
+    "kpool_16x8192_d128_p4": KPoolSpec("kpool_16x8192_d128_p4", [8192] * 16, pool=4, d=128),
+    "kpool_ragged_d128_p4": KPoolSpec("kpool_ragged_d128_p4", None, pool=4, d=128,
+                                      pad_rows=1024, max_lead=7),
+    "kpool_64x8192_d128_p4": KPoolSpec("kpool_64x8192_d128_p4", [8192] * 64, pool=4, d=128),
+}
+
+
+def make_kpool(spec: KPoolSpec | str, *, lengths: Optional[List[int]] = None,
+               leads: Optional[List[int]] = None, pool: Optional[int] = None,
+               d: Optional[int] = None, pad_rows: Optional[int] = None,
+               seed: Optional[int] = None, gate_scale: Optional[float] = None) -> KPoolPack:
+    """Draw a KPool pack; the keyword arguments override the spec (for tests)."""
+    if isinstance(spec, str):
+        spec = KPOOL_SPECS[spec]
+    if lengths is None:
+        if spec.lengths is not None:
+            lengths = spec.lengths
+        else:
+            u = uniforms(stream_key(spec.length_seed, TAG_LENGTHS), 0, spec.n_drawn_segments)
+            lengths = [int(1 + np.floor(x * spec.max_drawn_length)) for x in u]
+    P = spec.pool if pool is None else pool
+    d = spec.d if d is None else d
+    pad = spec.pad_rows if pad_rows is None else pad_rows
+    seed = spec.seed if seed is None else seed
+    gscale = spec.gate_scale if gate_scale is None else gate_scale
+    cu = np.zeros(len(lengths) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64))
+    capacity = int(cu[-1]) + pad
+    lead = None
+    if leads is None:
+        leads = spec.leads
+    if leads is not None:
+        lead = np.asarray(leads, dtype=np.int32)
+    elif spec.max_lead > 0:
+        u = uniforms(stream_key(seed, TAG_LEAD), 0, len(lengths))
+        lead = np.floor(u * (spec.max_lead + 1)).astype(np.int32)
+    key = f32_to_bf16_bits(normals(stream_key(seed, TAG_KEY), capacity * d).astype(np.float32))
+    gate = f32_to_bf16_bits(normals(stream_key(seed, TAG_GATE), capacity * d).astype(np.float32))
+    if gscale != 1.0:
+        gate = f32_to_bf16_bits(bf16_bits_to_f32(gate) * np.float32(gscale))
+    return KPoolPack(spec.name, P, d, capacity, cu, lead, key.reshape(capacity, d),
+                     gate.reshape(capacity, d))
+
+
+def make_kpool_custom(lengths: List[int], pool: int, d: int, *, leads: Optional[List[int]] = None,
+                      pad_rows: int = 0, seed: int = 0, gate_scale: float = 1.0) -> KPoolPack:
+    """A KPool pack with explicit segment lengths (and leads)."""
+    spec = KPoolSpec("kpool_custom", list(lengths), pool=pool, d=d, pad_rows=pad_rows,
+                     gate_scale=gate_scale, seed=seed)
+    return make_kpool(spec, leads=leads)
+
+
+def kpool_to_torch(pack: KPoolPack, device="cuda") -> Dict[str, "object"]:
+    """Uploads a KPool pack to torch tensors on ``device``."""
+    import torch
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    t = {"key": bf(pack.key).to(device), "gate": bf(pack.gate).to(device),
+         "cu_seqlens": torch.from_numpy(np.ascontiguousarray(pack.cu_seqlens)).to(device)}
+    if pack.lead is not None:
+        t["lead"] = torch.from_numpy(np.ascontiguousarray(pack.lead)).to(device)
+    return t
+
