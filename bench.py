@@ -18,6 +18,10 @@ under torch.distributed.run, or, when started without it, by relaunching itself 
 it with N processes. Timing is the max over ranks, and the value is the bytes of all
 ranks over that time. Rank 0 prints one JSON line.
 --impl reference times the fp64 CPU oracle on all host cores instead (rank 0 only).
+
+KPool configs (``--config kpool_*``, the DSA indexer's key pooling): one step is one
+csa_kpool_fwd call (default FP32 mode; the key-dtype compression mode is timed beside
+it); the same two passes, e2e, clocks, roofline and CPU baseline.
 """
 from __future__ import annotations
 
@@ -37,6 +41,7 @@ sys.path.insert(0, ROOT)
 import thd_synth as ts  # noqa: E402
 
 METRIC = "fwd+bwd µs and achieved HBM GB/s (% of GB300 roofline) per THD pack"
+KPOOL_METRIC = "KPool forward µs and achieved HBM GB/s (% of GB300 roofline) per THD key pack"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
@@ -45,14 +50,15 @@ L2_FLUSH_BYTES = 256 << 20
 # not the target). vs_baseline = our GB/s / (the same algorithmic bytes / that time).
 PAGE_FWD_BWD_US = {"1x8192_d128": 4.5 + 12.8, "3x8192_d128": 10.0 + 22.2,
                    "1x8192_d512": 12.4 + 22.8, "3x8192_d512": 35.0 + 66.0}
-# DRAM bytes per backward call, from one ncu capture of the current pooling kernel (the
-# summaries are kept with the profiles): its DRAM reads (dram__bytes_read.sum) plus the
-# bytes it writes into L2 (lts__t_sectors_srcunit_tex_op_write.sum x 32, all of which
-# reach DRAM, also the part still dirty in L2 when the kernel ends), plus the dAPE partials
-# the reduction kernel reads (row groups x ratio x coff*d x 4 bytes). Re-measured whenever
-# a kernel changes.
+# DRAM bytes per call of the roofline's kernel, from one ncu capture of the current
+# kernel (the summaries are kept with the profiles): its DRAM reads (dram__bytes_read.sum)
+# plus the bytes it writes into L2 (lts__t_sectors_srcunit_tex_op_write.sum x 32, all of
+# which reach DRAM, also the part still dirty in L2 when the kernel ends), plus, for the
+# compressor's backward call, the dAPE partials the reduction kernel reads (row groups x
+# ratio x coff*d x 4 bytes). Re-measured whenever a kernel changes.
 ROOFLINE_TRAFFIC = {"3x8192_d512": 108.269312e6 + 3223553 * 32 + 152 * 4 * 1024 * 4,
-                    "long_r128_d512": 136.89856e6 + 4349953 * 32 + 19 * 128 * 512 * 4}
+                    "long_r128_d512": 136.89856e6 + 4349953 * 32 + 19 * 128 * 512 * 4,
+                    "kpool_64x8192_d128_p4": 268.505856e6 + 1048576 * 32}
 
 
 # ----------------------------------------------------------------------------------
@@ -453,6 +459,267 @@ def run_e2e(args, pack, t, dev, alg_bytes, wsb):
 
 
 # ----------------------------------------------------------------------------------
+# KPool arm
+# ----------------------------------------------------------------------------------
+
+def kpool_bytes(pack) -> int:
+    """Algorithmic bytes of one KPool forward: every pooled key and gate element read once
+    (2 + 2 bytes), one bf16 output row per pool, cu_seqlens and the leads."""
+    pooled = pack.total_pools * pack.pool * pack.d
+    lead = 0 if pack.lead is None else 4 * pack.S
+    return 4 * pooled + 2 * pack.total_pools * pack.d + 4 * (pack.S + 1) + lead
+
+
+def kpool_workload_name(pack) -> str:
+    lens = np.diff(pack.cu_seqlens)
+    return (f"{pack.name}: THD key pack S={pack.S} keys={int(lens.sum())} capacity={pack.capacity} "
+            f"pool={pack.pool} d={pack.d} pools={pack.total_pools} "
+            f"leads={'none' if pack.lead is None else 'per segment'}")
+
+
+def run_ours_kpool(args, rank, world, local_rank):
+    import torch
+    import gated_pooling_gb300 as gp
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gp.load()
+    pack = ts.make_kpool(args.config)
+    nbytes = kpool_bytes(pack)
+    TC, d = pack.total_pools, pack.d
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def buffer_set(inputs):
+        return {"in": inputs, "out": torch.empty((TC, d), dtype=torch.bfloat16, device=dev)}
+
+    def set_bytes(bs):
+        return sum(x.numel() * x.element_size() for x in list(bs["in"].values()) + [bs["out"]])
+
+    base = buffer_set(ts.kpool_to_torch(pack, dev))
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (132 << 20))
+    n_sets = min(max(args.rotate, -(-2 * l2 // set_bytes(base))), max(args.rotate, 64))
+    sets = [base] + [buffer_set({k: v.clone() for k, v in base["in"].items()})
+                     for _ in range(n_sets - 1)]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush_rd.sum()
+
+    def call(bs, compress=0):
+        t = bs["in"]
+        gp.csa_kpool_fwd(t["key"], t["gate"], t["cu_seqlens"], t.get("lead"), pack.S, pack.pool,
+                         d, pack.capacity, bs["out"], TC, compress, err, stream=sp)
+
+    for k in range(max(args.warmup, n_sets)):
+        flush_l2()
+        call(sets[k % n_sets])
+        call(sets[k % n_sets], 1)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())}")
+
+    def new_events(n):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", local_rank))
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    if rank == 0:
+        sampler.start()
+
+    def bracket():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    sev = [new_events(2) for _ in range(args.steps)]
+    bracket()
+    for k in range(args.steps):
+        flush_l2()
+        sev[k][0].record(stream)
+        call(base)
+        sev[k][1].record(stream)
+    bracket()
+
+    def steady(compress):
+        a, b = new_events(2)
+        bracket()
+        a.record(stream)
+        for k in range(args.steps):
+            call(sets[k % n_sets], compress)
+        b.record(stream)
+        bracket()
+        return a.elapsed_time(b)
+
+    steady_total = steady(0)
+    steady_c_total = steady(1)
+    clocks = sampler.stop() if rank == 0 else None
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())}")
+    step_ms = [sev[k][0].elapsed_time(sev[k][1]) for k in range(args.steps)]
+    total_ms, st_ms, stc_ms = max_over_ranks([sum(step_ms), steady_total, steady_c_total],
+                                             device=dev)
+    flushed_ms = total_ms / args.steps
+    steady_ms = st_ms / args.steps
+    compress_ms = stc_ms / args.steps
+    ms_step = max(flushed_ms, steady_ms)
+    value = whole_job_gbs(world, nbytes, ms_step)
+    e2e = run_kpool_e2e(args, pack, base["in"], dev, nbytes) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_hbm_peak()
+    call_gbs = nbytes / (steady_ms * 1e-3) / 1e9
+    per_gpu = lambda ms: nbytes / (ms * 1e-3) / 1e9
+    res = {
+        "metric": KPOOL_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": kpool_workload_name(pack), "pool": pack.pool, "d": d,
+                   "S": pack.S, "capacity": pack.capacity, "pools": TC, "mode": "fp32 weighted sum",
+                   "l2": (f"value = the slower of two passes: (flushed) L2 flushed before every "
+                          f"call outside the timed events; (steady) back-to-back calls rotating "
+                          f"over {n_sets} buffer sets of {set_bytes(base) / 1e6:.1f} MB "
+                          + (f"(> 2x the {l2 >> 20} MiB L2)" if n_sets * set_bytes(base) > 2 * l2
+                             else f"(together smaller than the {l2 >> 20} MiB L2)") + ", no flush"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "flushed": {"us_per_step": round(flushed_ms * 1e3, 2),
+                    "gbs_per_gpu": round(per_gpu(flushed_ms), 1)},
+        "steady": {"us_per_step": round(steady_ms * 1e3, 2),
+                   "gbs_per_gpu": round(per_gpu(steady_ms), 1), "buffer_sets": n_sets,
+                   "set_bytes": set_bytes(base)},
+        "compress_us": round(compress_ms * 1e3, 2),
+        "compress_gbs": round(per_gpu(compress_ms), 1),
+        "bytes": nbytes,
+        "frac_of_measured_hbm": round(value / world / peak, 4),
+        "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "kernel": "csa_kpool_fwd (one pooling kernel)",
+                     "achieved": round(call_gbs, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(call_gbs / peak, 4),
+                     "traffic": ROOFLINE_TRAFFIC.get(args.config)},
+        "e2e": e2e, "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = kpool_cpu_baseline(pack, budget_s=args.cpu_seconds)
+    return res
+
+
+def run_kpool_e2e(args, pack, t, dev, alg_bytes):
+    """KPool through the public API with host buffers: each step copies the keys, gates,
+    cu_seqlens and leads in from pinned host memory, pools, and copies the pooled keys back;
+    pipelined over two device buffer sets on three streams like the compressor's e2e."""
+    import torch
+    import gated_pooling_gb300 as gp
+
+    TC, d = pack.total_pools, pack.d
+    host = {k: v.cpu().pin_memory() for k, v in t.items()}
+    h_out = torch.empty((TC, d), dtype=torch.bfloat16).pin_memory()
+    slots = [{"in": {k: torch.empty_like(v) for k, v in t.items()},
+              "out": torch.empty((TC, d), dtype=torch.bfloat16, device=dev),
+              "h2d_done": torch.cuda.Event(), "comp_done": torch.cuda.Event(),
+              "d2h_done": torch.cuda.Event()} for _ in range(2)]
+    s_h2d, s_comp, s_d2h = (torch.cuda.Stream(dev) for _ in range(3))
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = h_out.numel() * h_out.element_size()
+
+    def step(k):
+        sl = slots[k % 2]
+        with torch.cuda.stream(s_h2d):
+            if k >= 2:
+                s_h2d.wait_event(sl["comp_done"])
+            for name, buf in sl["in"].items():
+                buf.copy_(host[name], non_blocking=True)
+            sl["h2d_done"].record(s_h2d)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(sl["h2d_done"])
+            if k >= 2:
+                s_comp.wait_event(sl["d2h_done"])
+            x = sl["in"]
+            gp.csa_kpool_fwd(x["key"], x["gate"], x["cu_seqlens"], x.get("lead"), pack.S,
+                             pack.pool, d, pack.capacity, sl["out"], TC, 0, None,
+                             stream=s_comp.cuda_stream)
+            sl["comp_done"].record(s_comp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(sl["comp_done"])
+            h_out.copy_(sl["out"], non_blocking=True)
+            sl["d2h_done"].record(s_d2h)
+
+    for k in range(4):
+        step(k)
+    torch.cuda.synchronize()
+    n = args.e2e_steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_h2d)
+    for k in range(n):
+        step(k)
+    s_d2h.wait_stream(s_h2d)
+    b.record(s_d2h)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    return {"value": round(alg_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelined": "two buffer sets; input copy, call and output copy on three streams"}
+
+
+def kpool_oracle_seconds(pack, threads: int) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.kpool_fwd_pack(pack, nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def kpool_cpu_baseline(pack, budget_s=12.0):
+    """The KPool oracle as it stands, on all host cores (std::thread over pool ranges) on
+    the whole pack; `value` is that figure."""
+    import oracle
+    cores = oracle.hardware_threads()
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while not times or (time.perf_counter() < t_end and len(times) < 10):
+        times.append(kpool_oracle_seconds(pack, cores))
+    sec = statistics.median(times)
+    return {"value": round(kpool_bytes(pack) / sec / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"the whole pack, FP32 mode on {cores} host threads (pool ranges), "
+                      f"x{len(times)}, median {sec:.3f} s per call"}
+
+
+def run_reference_kpool(args, rank):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    cores = oracle.hardware_threads()
+    pack = ts.make_kpool(args.config)
+    for _ in range(args.warmup):
+        kpool_oracle_seconds(pack, cores)
+    times = [kpool_oracle_seconds(pack, cores) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = kpool_bytes(pack) / (ms * 1e-3) / 1e9
+    desc = f"fp64 KPool oracle on {cores} host threads (pool ranges), the whole pack per step"
+    return {"impl": "reference", "metric": KPOOL_METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": kpool_workload_name(pack), "pool": pack.pool, "d": pack.d,
+                       "S": pack.S, "capacity": pack.capacity, "pools": pack.total_pools,
+                       "mode": "fp32 weighted sum"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------------
 # CPU oracle (baseline leg and the reference arm)
 # ----------------------------------------------------------------------------------
 
@@ -575,7 +842,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default=ts.HEADLINE, choices=sorted(ts.SPECS))
+    ap.add_argument("--config", default=ts.HEADLINE, choices=sorted(ts.SPECS) + sorted(ts.KPOOL_SPECS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rotate", type=int, default=3,
                     help="minimum buffer sets the steady pass rotates over")
@@ -598,14 +865,15 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    kpool = args.config in ts.KPOOL_SPECS
     if args.impl == "reference":
-        res = run_reference(args, rank)
+        res = run_reference_kpool(args, rank) if kpool else run_reference(args, rank)
     else:
         if world > 1:
             import torch
             torch.cuda.set_device(local_rank)
             torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-        res = run_ours(args, rank, world, local_rank)
+        res = (run_ours_kpool if kpool else run_ours)(args, rank, world, local_rank)
         if world > 1:
             import torch
             torch.distributed.destroy_process_group()

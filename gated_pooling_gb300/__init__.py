@@ -5,9 +5,9 @@ below have the C names and arguments, and only marshal them (tensor -> device
 pointer, stream -> cudaStream_t). Every step of the pooling runs in the library's
 CUDA kernels. There is no fallback: if the library is missing, loading raises.
 
-Tensors are torch CUDA tensors (bf16 for kv/score/dout/out/dkv/dscore, fp32 for
-ape/dape, int32 for cu_seqlens and the error word); PyTorch only provides device
-memory and streams.
+Tensors are torch CUDA tensors (bf16 for kv/score/dout/out/dkv/dscore and the KPool
+key/gate, fp32 for ape/dape, int32 for cu_seqlens, lead and the error word); PyTorch
+only provides device memory and streams.
 """
 from __future__ import annotations
 
@@ -21,12 +21,13 @@ LIB_PATH = _build.LIB
 _lib: Optional[ctypes.CDLL] = None
 
 CSA_OK, CSA_ERR_INVALID_VALUE, CSA_ERR_UNSUPPORTED, CSA_ERR_WORKSPACE, CSA_ERR_CUDA = 0, 1, 2, 3, 4
-CSA_DEVERR_CU_SEQLENS, CSA_DEVERR_OUT_ROWS, CSA_DEVERR_TIMEOUT = 1, 2, 3
+CSA_DEVERR_CU_SEQLENS, CSA_DEVERR_OUT_ROWS, CSA_DEVERR_TIMEOUT, CSA_DEVERR_LEAD = 1, 2, 3, 4
 CSA_TEST_MIN_WAIT_CYCLES = 1000000
+CSA_KPOOL_MAX_POOL = 1024
 EXPORTED = ("csa_status_string", "csa_last_error_string", "csa_compressor_total_comp", "csa_compressor_fwd",
             "csa_compressor_bwd_workspace_bytes", "csa_compressor_bwd",
             "csa_compressor_bwd_noalloc", "csa_compressor_test_hooks",
-            "csa_compressor_map_blocks")
+            "csa_compressor_map_blocks", "csa_kpool_total", "csa_kpool_fwd")
 
 
 class CsaError(RuntimeError):
@@ -69,6 +70,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_compressor_test_hooks.argtypes = [i64, i32]
     lib.csa_compressor_map_blocks.restype = ctypes.c_int
     lib.csa_compressor_map_blocks.argtypes = [vp, i32, i32, i64, i64, vp, vp, vp]
+    lib.csa_kpool_total.restype = i64
+    lib.csa_kpool_total.argtypes = [vp, vp, i32, i32]
+    lib.csa_kpool_fwd.restype = ctypes.c_int
+    lib.csa_kpool_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i64, vp, i64, i32, vp, vp]
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -162,3 +167,27 @@ def csa_compressor_map_blocks(cu_seqlens, S: int, ratio: int, capacity: int, out
     _check(load().csa_compressor_map_blocks(_ptr(cu_seqlens), S, ratio, capacity, out_rows,
                                             _ptr(seg_blk_base), _ptr(dev_error),
                                             _stream(stream)), "csa_compressor_map_blocks")
+
+
+def csa_kpool_total(cu_seqlens_host, lead_host, S: int, pool: int) -> int:
+    """Pool count from host int32 arrays (``lead_host`` may be None)."""
+    import numpy as np
+    def arr(x):
+        if x is None:
+            return None
+        if hasattr(x, "numpy"):
+            x = x.numpy()
+        return np.ascontiguousarray(x, dtype=np.int32)
+    cu, ld = arr(cu_seqlens_host), arr(lead_host)
+    return int(load().csa_kpool_total(cu.ctypes.data_as(ctypes.c_void_p),
+                                      None if ld is None else ld.ctypes.data_as(ctypes.c_void_p),
+                                      S, pool))
+
+
+def csa_kpool_fwd(key, gate, cu_seqlens, lead, S: int, pool: int, d: int, capacity: int, out,
+                  out_rows: int, compress: int = 0, dev_error=None, stream=None) -> None:
+    """KPool forward (the DSA indexer's key pooling); ``lead`` may be None."""
+    _check(load().csa_kpool_fwd(_ptr(key), _ptr(gate), _ptr(cu_seqlens), _ptr(lead), S, pool, d,
+                                capacity, _ptr(out), out_rows, int(compress), _ptr(dev_error),
+                                _stream(stream)), "csa_kpool_fwd")
+

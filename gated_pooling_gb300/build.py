@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libcsa_compressor.so")
-SOURCES = ["csa_fwd.cu", "csa_bwd.cu", "csa_api.cu", "csa_noalloc.cu"]
+SOURCES = ["csa_fwd.cu", "csa_bwd.cu", "csa_api.cu", "csa_noalloc.cu", "csa_kpool.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

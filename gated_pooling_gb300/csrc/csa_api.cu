@@ -33,6 +33,8 @@ thread_local cudaError_t t_last_error = cudaSuccess;
 std::atomic<long long> g_wait_cycles{kWaitCycles};
 std::atomic<int> g_withhold_row{-1};
 
+}  // namespace
+
 // Records a failing CUDA call for csa_last_error_string() and passes the code on.
 cudaError_t note(cudaError_t e) {
   if (e != cudaSuccess) t_last_error = e;
@@ -85,6 +87,8 @@ cudaError_t blocks_per_sm(int dev, const void* kernel, int threads, size_t smem,
   *blocks = n;
   return cudaSuccess;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -227,6 +231,8 @@ PoolParams base_params(const Plan& pl, const void* kv, const void* score, const 
   return p;
 }
 
+}  // namespace
+
 // Every pooling kernel is launched as a programmatic dependent of the stream's previous
 // kernel (it waits for that grid inside build_block_prefix before touching memory).
 #ifndef CSA_PDL_POOL
@@ -246,6 +252,8 @@ cudaError_t launch_pdl(const void* k, dim3 grid, dim3 block, size_t smem, cudaSt
   cfg.numAttrs = 1;
   return note(cudaLaunchKernelExC(&cfg, k, args));
 }
+
+namespace {
 
 csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t stream) {
   if (pl.longk) {

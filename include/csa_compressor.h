@@ -69,12 +69,14 @@ typedef enum {
 #define CSA_DEVERR_TIMEOUT 3    /* a wait for an asynchronous copy gave up (about 2 s); the
                                    kernel stopped early, outputs (dAPE included) are
                                    incomplete */
+#define CSA_DEVERR_LEAD 4       /* KPool: a negative lead */
 
 /* Limits checked on the host (CSA_ERR_UNSUPPORTED beyond them). */
 #define CSA_MAX_SEGMENTS 16384   /* S */
 #define CSA_MAX_WINDOW 2048      /* coff * ratio */
 #define CSA_MAX_GENERIC_WINDOW 256 /* coff * ratio when d % 8 != 0 or a pointer is not 16-byte aligned */
 #define CSA_MAX_ELEMS 2147483647 /* capacity*coff*d and out_rows*d must stay below 2^31 */
+#define CSA_KPOOL_MAX_POOL 1024  /* KPool pool size */
 
 /* Text for a status code (static storage). */
 const char* csa_status_string(int status);
@@ -178,6 +180,50 @@ csa_status_t csa_compressor_test_hooks(int64_t wait_cycles, int32_t withhold_row
 csa_status_t csa_compressor_map_blocks(const int32_t* cu_seqlens, int32_t S, int32_t ratio,
                                        int64_t capacity, int64_t out_rows, int32_t* seg_blk_base,
                                        int32_t* dev_error, csa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * KPool: the DSA indexer's key pooling ("Megatron-LM PR #8835", the KPool commits: the
+ * one adding dsa_indexer_kpool_key_dtype_compression and the explicit-mask pool origin,
+ * and the one with the empty-query guard; KPool selection is NVIDIA#8287 there).
+ *
+ *   Segment s covers keys [cu_seqlens[s], cu_seqlens[s+1]); its first valid key is
+ *   f = cu_seqlens[s] + lead[s] (lead NULL: 0). Its keys from f on are grouped into
+ *   pools of `pool` consecutive keys, the grid restarting at every segment; the
+ *   fewer-than-pool keys after its last complete pool form no pool (tail selection, which
+ *   appends them individually, is part of the selection, not of this pooling). Output
+ *   rows are the pools of all segments in order (csa_kpool_total rows).
+ *   For a pool and column j < d: an FP32 softmax of gate[t, j] over the pool's keys t
+ *   weights key[t, j]:
+ *     compress = 0: out = bf16(sum_t p_t key[t, j]), the sum in fp32;
+ *     compress = 1 (key-dtype compression): each weight is cast to bf16 before
+ *       multiplying and reducing: out = bf16(sum_t bf16(bf16(p_t) * key[t, j])), the sum
+ *       of the bf16 products in fp32.
+ *   Forward only: the selection that consumes the pooled keys records no gradient.
+ * ------------------------------------------------------------------------------------ */
+
+/* Number of pools: sum over s of floor(max(0, cu[s+1] - cu[s] - lead[s]) / pool), from
+ * HOST copies of cu_seqlens [S+1] and lead [S] (lead may be NULL). Returns -1 when
+ * cu_seqlens is NULL, S < 0, pool < 1, the offsets decrease or a lead is negative. */
+int64_t csa_kpool_total(const int32_t* cu_seqlens_host, const int32_t* lead_host, int32_t S,
+                        int32_t pool);
+
+/* KPool forward.
+ *   key, gate   bf16 [capacity, d] (device)
+ *   cu_seqlens  int32 [S+1] (device), non-decreasing, cu_seqlens[S] <= capacity
+ *   lead        int32 [S] (device), >= 0, or NULL (every segment starts at cu_seqlens[s];
+ *               a lead at or past the segment's end leaves it without pools)
+ *   pool        1 .. CSA_KPOOL_MAX_POOL
+ *   out         bf16 [out_rows, d] (device); rows >= the pool count are not written
+ *   compress    0 or 1 (see above)
+ *   dev_error   int32 (device) or NULL: CSA_DEVERR_CU_SEQLENS, CSA_DEVERR_LEAD or
+ *               CSA_DEVERR_OUT_ROWS (more pools than out_rows); nothing is written then
+ * The vector kernel runs when d is a multiple of 8, pool <= 8 and key, gate and out are
+ * 16-byte aligned; anything else takes a scalar kernel. One kernel is enqueued (none when
+ * S = 0). Status codes as for the compressor. */
+csa_status_t csa_kpool_fwd(const void* key, const void* gate, const int32_t* cu_seqlens,
+                           const int32_t* lead, int32_t S, int32_t pool, int32_t d,
+                           int64_t capacity, void* out, int64_t out_rows, int32_t compress,
+                           int32_t* dev_error, csa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -48,7 +48,7 @@ def test_status_codes_match_header():
         m = re.search(rf"\b{name} = (\d+)", text)
         assert m and int(m.group(1)) == getattr(gp, name), name
     for name in ("CSA_DEVERR_CU_SEQLENS", "CSA_DEVERR_OUT_ROWS", "CSA_DEVERR_TIMEOUT",
-                 "CSA_TEST_MIN_WAIT_CYCLES"):
+                 "CSA_DEVERR_LEAD", "CSA_TEST_MIN_WAIT_CYCLES", "CSA_KPOOL_MAX_POOL"):
         m = re.search(rf"#define {name} (\d+)", text)
         assert m and int(m.group(1)) == getattr(gp, name), name
 
@@ -149,3 +149,49 @@ def test_map_blocks_rejects(lib):
     assert lib.csa_compressor_map_blocks(None, 1, 4, 8, 2, FAKE, None, None) == gp.CSA_ERR_INVALID_VALUE
     assert lib.csa_compressor_map_blocks(FAKE, 1, 0, 8, 2, FAKE, None, None) == gp.CSA_ERR_INVALID_VALUE
     assert lib.csa_compressor_map_blocks(FAKE, 1, 4, 8, 2, None, None, None) == gp.CSA_ERR_INVALID_VALUE
+
+
+def test_kpool_total_host_helper(lib, oracle_lib):
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        S = int(rng.integers(0, 9))
+        cu = np.concatenate([[0], np.cumsum(rng.integers(0, 40, S))]).astype(np.int32)
+        lead = rng.integers(0, 12, S).astype(np.int32) if rng.random() < 0.7 else None
+        P = int(rng.integers(1, 9))
+        assert gp.csa_kpool_total(cu, lead, S, P) == oracle.kpool_total(cu, lead, P)
+    assert gp.csa_kpool_total(np.array([0, 5, 3], np.int32), None, 2, 2) == -1
+    assert gp.csa_kpool_total(np.array([0, 5], np.int32), np.array([-1], np.int32), 1, 2) == -1
+    assert gp.csa_kpool_total(np.array([0, 5], np.int32), None, 1, 0) == -1
+
+
+def kpool_status(lib, **over):
+    a = dict(key=FAKE, gate=FAKE, cu=FAKE, lead=None, S=1, pool=4, d=8, capacity=8, out=FAKE,
+             out_rows=2, compress=0, err=None)
+    a.update(over)
+    return lib.csa_kpool_fwd(a["key"], a["gate"], a["cu"], a["lead"], a["S"], a["pool"], a["d"],
+                             a["capacity"], a["out"], a["out_rows"], a["compress"], a["err"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(S=-1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(pool=0), gp.CSA_ERR_INVALID_VALUE),
+    (dict(d=0), gp.CSA_ERR_INVALID_VALUE),
+    (dict(capacity=-1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(out_rows=-1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(compress=2), gp.CSA_ERR_INVALID_VALUE),
+    (dict(cu=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(key=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(gate=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(out=None), gp.CSA_ERR_INVALID_VALUE),
+    (dict(key=FAKE + 1), gp.CSA_ERR_INVALID_VALUE),
+    (dict(lead=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),
+    (dict(err=FAKE + 2), gp.CSA_ERR_INVALID_VALUE),
+    (dict(S=20000), gp.CSA_ERR_UNSUPPORTED),
+    (dict(pool=gp.CSA_KPOOL_MAX_POOL + 1), gp.CSA_ERR_UNSUPPORTED),
+    (dict(capacity=1 << 28, d=64), gp.CSA_ERR_UNSUPPORTED),
+    (dict(out_rows=1 << 28, d=64), gp.CSA_ERR_UNSUPPORTED),
+    (dict(S=0), gp.CSA_OK),  # no segment: nothing to enqueue
+])
+def test_kpool_rejects(lib, over, code):
+    assert kpool_status(lib, **over) == code
+
