@@ -32,7 +32,6 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
                                     warp_sums, sCu);
   publish_status(p, TC);
   if (TC < 0) return;
-  pdl_trigger();  // the next kernel of the stream may launch
 
   const int tid = threadIdx.x;
   const int d = p.d, C = p.C, V = p.V;
