@@ -146,8 +146,9 @@ __device__ __forceinline__ int block_exclusive_scan(int val, int* warp_sums, int
 // Programmatic dependent launch. The kernels are launched as programmatic dependents of
 // the previous kernel of their stream; pdl_wait (the first thing the map builders do,
 // before any global memory access) holds them until that grid has completed and its
-// memory is visible. It returns at once when the kernel was launched normally. The pooling
-// kernels do not trigger their own dependents early (measured slower); KPool does.
+// memory is visible. It returns at once when the kernel was launched normally. No kernel
+// of this library triggers its own dependents early (measured slower): the next kernel
+// starts when the grid ends.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Lets the next kernel of the stream, if launched as a programmatic dependent, begin its
 // launch (it still waits for this grid's completion before touching memory).

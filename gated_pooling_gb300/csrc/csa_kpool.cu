@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kKpThreads, PT <= 2 ? 3 : (PT <= 4 ? 2 : 1))
   int* sF = sB + p.sB_words;
   const int TC = build_pool_prefix(p, sB, sF, warp_sums);
   if (TC < 0) return;
-  pdl_trigger();  // the next kernel of the stream may launch
+  // (no early launch of the stream's next kernel: measured slower, as for the pooling)
 
   const int g = blockIdx.x;
   const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
@@ -217,7 +217,6 @@ __global__ void __launch_bounds__(kKpThreads) kpool_scalar_kernel(const KPoolPar
   int* sF = sB + p.sB_words;
   const int TC = build_pool_prefix(p, sB, sF, warp_sums);
   if (TC < 0) return;
-  pdl_trigger();
 
   const int g = blockIdx.x;
   const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
