@@ -150,11 +150,6 @@ __device__ __forceinline__ int block_exclusive_scan(int val, int* warp_sums, int
 // of this library triggers its own dependents early (measured slower): the next kernel
 // starts when the grid ends.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Lets the next kernel of the stream, if launched as a programmatic dependent, begin its
-// launch (it still waits for this grid's completion before touching memory).
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Builds the block prefix sB[s] = sum_{s' < s} floor(L_s' / ratio), s = 0..S, in shared
 // memory and returns total_comp = sB[S]. Checks cu_seqlens (cu[0] >= 0, non-decreasing,
