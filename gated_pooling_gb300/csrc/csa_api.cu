@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include <cuda.h>
@@ -284,21 +285,22 @@ csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t st
 }
 
 // dAPE = (accumulate ? dAPE : 0) + sum over row groups g = 0..R-1 of partial[g]. A block
-// covers 32 entries with SPLIT warps; warp k adds the contiguous row-group range
-// [k*R/SPLIT, (k+1)*R/SPLIT) (loaded kReduceBatch at a time, so the loads overlap) with
-// compensated fp32 sums; the range sums are then combined pairwise in a fixed tree. SPLIT
-// follows R (about five partials per warp), so that few threads idle. The result is the
-// same bits on every run. Launched as a programmatic dependent of the pooling kernel: it
-// may start early and waits for that grid's results.
-constexpr int kReduceCols = 32;
+// covers COLS entries (one per lane group) with SPLIT thread groups; group k adds the
+// contiguous row-group range [k*R/SPLIT, (k+1)*R/SPLIT) (loaded kReduceBatch at a time, so
+// the loads overlap) with compensated fp32 sums; the range sums are then combined pairwise
+// in a fixed tree. SPLIT follows R (about five partials per group, ten when R is small),
+// COLS is 16 when there are few entries (more blocks); both measured on GB300. The result
+// is the same bits on every run. Launched as a programmatic dependent of the pooling
+// kernel: it waits for that grid's results.
 constexpr int kReduceBatch = 12;  // partials a thread has in flight at once
 // A non-zero status word (the pooling kernel found cu_seqlens or out_rows invalid) leaves
 // dAPE untouched.
-template <int SPLIT>
-__global__ void __launch_bounds__(kReduceCols * SPLIT)
+template <int SPLIT, int COLS>
+__global__ void __launch_bounds__(COLS * SPLIT)
     dape_reduce_kernel(const float* __restrict__ partial, int R, int n, float* __restrict__ dape,
                        int accumulate, const int32_t* __restrict__ status) {
   constexpr int kReduceSplit = SPLIT;
+  constexpr int kReduceCols = COLS;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // read with the partials (only the final write depends on it)
   const int32_t call_status = *reinterpret_cast<const volatile int32_t*>(status);
@@ -492,17 +494,26 @@ csa_status_t csa_compressor_bwd(const void* kv, const void* score, const float* 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  // warps per block: the power of two nearest above R/5, at most 32
+  // thread groups per block: the power of two nearest above R/5 (R/10 when R is below 32),
+  // at most 32; 16 entries per block when 32-entry blocks would be fewer than 64
+  const int per = R < 32 ? 10 : 5;
   int split = 1;
-  while (split < 32 && split * 5 < R) split *= 2;
-  const void* rk = split == 1    ? reinterpret_cast<const void*>(dape_reduce_kernel<1>)
-                   : split == 2  ? reinterpret_cast<const void*>(dape_reduce_kernel<2>)
-                   : split == 4  ? reinterpret_cast<const void*>(dape_reduce_kernel<4>)
-                   : split == 8  ? reinterpret_cast<const void*>(dape_reduce_kernel<8>)
-                   : split == 16 ? reinterpret_cast<const void*>(dape_reduce_kernel<16>)
-                                 : reinterpret_cast<const void*>(dape_reduce_kernel<32>);
-  cfg.gridDim = dim3((n + kReduceCols - 1) / kReduceCols);
-  cfg.blockDim = dim3(kReduceCols * split);
+  while (split < 32 && split * per < R) split *= 2;
+  const bool narrow = (n + 31) / 32 < 64;
+  const int cols = narrow ? 16 : 32;
+  auto pick = [&](auto c) -> const void* {
+    constexpr int C = decltype(c)::value;
+    return split == 1    ? reinterpret_cast<const void*>(dape_reduce_kernel<1, C>)
+           : split == 2  ? reinterpret_cast<const void*>(dape_reduce_kernel<2, C>)
+           : split == 4  ? reinterpret_cast<const void*>(dape_reduce_kernel<4, C>)
+           : split == 8  ? reinterpret_cast<const void*>(dape_reduce_kernel<8, C>)
+           : split == 16 ? reinterpret_cast<const void*>(dape_reduce_kernel<16, C>)
+                         : reinterpret_cast<const void*>(dape_reduce_kernel<32, C>);
+  };
+  const void* rk = narrow ? pick(std::integral_constant<int, 16>{})
+                          : pick(std::integral_constant<int, 32>{});
+  cfg.gridDim = dim3((n + cols - 1) / cols);
+  cfg.blockDim = dim3(cols * split);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cfg.attrs = attr;
