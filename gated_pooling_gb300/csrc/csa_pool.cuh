@@ -673,11 +673,20 @@ constexpr int kLongSliceCols = 64;  // columns per half in a long-window CTA sli
 #define CSA_LONG_BWD_GROUPS 2
 #endif
 
-// Consumer groups of the long-window kernel for a window of W positions: 256-position
-// windows (ratio 128 at coff 2) have 64 KB stages, of which only two or three fit, so they
-// run one group per direction.
+// Consumer groups of the long-window kernel for a window of W positions. 256-position
+// windows (ratio 128 at coff 2) have 64 KB stages, of which only two or three fit, so two
+// groups do not take alternate rows there: both take every row, each half of its positions
+// (the position split). The backward runs it (r128c2 d128: 57.6 -> 54.4 us); the forward
+// measured slower with it (20.5 -> 21.1 us) and runs one group.
+#ifndef CSA_LONG_W256_FWD_GROUPS
+#define CSA_LONG_W256_FWD_GROUPS 1
+#endif
+#ifndef CSA_LONG_W256_BWD_GROUPS
+#define CSA_LONG_W256_BWD_GROUPS 2
+#endif
 constexpr int long_groups(bool bwd, int W) {
-  return W >= 256 ? 1 : (bwd ? CSA_LONG_BWD_GROUPS : CSA_LONG_FWD_GROUPS);
+  return W >= 256 ? (bwd ? CSA_LONG_W256_BWD_GROUPS : CSA_LONG_W256_FWD_GROUPS)
+                  : (bwd ? CSA_LONG_BWD_GROUPS : CSA_LONG_FWD_GROUPS);
 }
 
 #ifndef CSA_LONG_W256
@@ -701,15 +710,21 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit
   pl.box_rows = r;
   pl.sB_words = ((S + 1) + 3) & ~3;
   const int ng = long_groups(bwd, W);
-  const bool ape_smem = bwd || ng > 1;  // else the forward keeps ape in registers
+  // the forward keeps ape in registers with one group, or with a 256-position window
+  const bool ape_smem = bwd || (ng > 1 && W < 256);
   const size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
-  const size_t ring_off = ape_off + (ape_smem ? (size_t)16 * (W + 4) * 16 : 0);
+  // the position split's column max and sums exchange ([3][2 groups][64 columns] floats)
+  // sits just below the ring
+  const size_t xch = (W >= 256 && ng == 2) ? (size_t)3 * 2 * kLongSliceCols * 4 : 0;
+  const size_t ring_off = ape_off + (ape_smem ? (size_t)16 * (W + 4) * 16 : 0) + xch;
   pl.stage_bytes = 2 * W * 128;
   // + the dout slice and 4 mbarriers (backward: two full, empty, done), 3 (forward)
   const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 + 32 : 24);
   if (smem_limit < ring_off + 1024 + 2 * per_stage) return false;
   const size_t depth = std::min<size_t>(16, (smem_limit - ring_off - 1024) / per_stage);
-  if (depth <= (size_t)ng) return false;  // every consumer group needs a stage of its own
+  // every consumer group needs a stage of its own (the groups of a 256-position window
+  // share theirs)
+  if (depth <= (size_t)(W >= 256 ? 1 : ng)) return false;
   pl.depth = (int)depth;
   pl.threads = ng * kThreads + (bwd ? 96 : 32);  // + producer warp (+ store and zero warps)
   pl.ape_off = (int)ape_off;

@@ -78,6 +78,40 @@ __device__ __forceinline__ void sts_words2(void* p, uint32_t a, uint32_t b) {
 // 128-byte swizzle (tile base on a 1024-byte boundary): the chunk is stored at c ^ (y mod 8).
 __device__ __forceinline__ int swz(int y, int c) { return y * 128 + ((c ^ (y & 7)) << 4); }
 
+// Named barrier `id` over n threads that also ANDs a predicate over them: every thread
+// gets the same answer.
+__device__ __forceinline__ bool bar_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// Column-pair arithmetic of the consumers: packed f32x2 instructions (PK), or the same
+// operations on each fp32 of the pair, which the compiler is free to schedule and contract
+// (a product and a sum into one fma) as scalar code.
+template <bool PK>
+__device__ __forceinline__ uint64_t c2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  if constexpr (PK) return f2_fma(a, b, c);
+  return f2_pack(fmaf(f2_lo(a), f2_lo(b), f2_lo(c)), fmaf(f2_hi(a), f2_hi(b), f2_hi(c)));
+}
+template <bool PK>
+__device__ __forceinline__ uint64_t c2_add(uint64_t a, uint64_t b) {
+  if constexpr (PK) return f2_add(a, b);
+  return f2_pack(f2_lo(a) + f2_lo(b), f2_hi(a) + f2_hi(b));
+}
+template <bool PK>
+__device__ __forceinline__ uint64_t c2_mul(uint64_t a, uint64_t b) {
+  if constexpr (PK) return f2_mul(a, b);
+  return f2_pack(f2_lo(a) * f2_lo(b), f2_hi(a) * f2_hi(b));
+}
+
 template <int PP, int NG, int COFF, bool BWD>
 __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     pool_long_kernel(const PoolParams p, const __grid_constant__ CUtensorMap tm_kv,
@@ -89,10 +123,25 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   constexpr int kTile = W * 128;      // one tensor's window in a stage
   constexpr int NCT = NG * kThreads;  // consumer threads
   static_assert(NG >= 1 && (!BWD || NG <= 2), "the dAPE combine handles two groups");
-  constexpr bool kApReg = !BWD && NG == 1;
-  // the backward recomputes the softmax terms from the staged tile in each pass when two
-  // groups share the registers, or when a lane owns 16 positions (256-position windows)
-  constexpr bool kRecomp = BWD && (NG > 1 || PP >= 16);
+  // 256-position windows with two groups: both groups take every row, group g the
+  // positions [128 g, 128 g + 128) (the previous block, then the own block), and they merge
+  // the column max and the sums through shared memory; other windows: the groups take
+  // alternate rows
+  constexpr bool kPS = NG == 2 && PP >= 16;
+  constexpr int PPG = kPS ? PP / 2 : PP;  // positions per lane in a row
+  constexpr int RSTEP = kPS ? 1 : NG;     // rows a group advances per iteration
+  constexpr bool kApReg = !BWD && (NG == 1 || kPS);  // forward: a lane's ape in registers
+  // packed f32x2 arithmetic where it measured faster: the forward of 256-position windows,
+  // whose single group of 8 warps is bound by instruction issue (r128c2 d128 forward 20.5
+  // -> 18.1 us); elsewhere it measured slower (up to +15 % for 64-position backwards)
+#ifndef CSA_LONG_PACKED
+#define CSA_LONG_PACKED 1  // 0: never, 1: 256-position forwards, 2: every instantiation
+#endif
+  constexpr bool kPk = CSA_LONG_PACKED == 2 || (CSA_LONG_PACKED == 1 && !BWD && PP >= 16);
+  // later passes recompute the softmax terms from the staged tile instead of keeping them in
+  // registers: in the backward when two groups share the registers or a lane owns 16
+  // positions, and with the position split (whose forward keeps ape in registers instead)
+  constexpr bool kRecomp = (BWD && (NG > 1 || PP >= 16)) || kPS;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   __shared__ int s_abort;
@@ -121,8 +170,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     for (int t = tid; t < nb; t += blockDim.x) {
       const int k = t / p.depth;
       if (k < 2) mbar_init(&full[t], 1);
-      else if (k == 2) mbar_init(&empty[t - 2 * p.depth], BWD ? 1 : kThreads);  // bwd: store warp
-      else mbar_init(&done[t - 3 * p.depth], kThreads);
+      else if (k == 2) mbar_init(&empty[t - 2 * p.depth], BWD ? 1 : (kPS ? NCT : kThreads));
+      else mbar_init(&done[t - 3 * p.depth], kPS ? NCT : kThreads);  // (bwd empty: store warp)
       fence_proxy_async_smem();
     }
     if (tid == 0) {
@@ -286,14 +335,15 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   const int ch = lane & 1;               // which 4 columns of the chunk
   const int cl = wi * 8 + ch * 4;        // first column of this thread inside the slice
 
-  // ape of this thread's slots, scaled by log2 e: registers, or shared memory as
-  // [4-column group][position] float4 (written by group 0; groups W + 4 apart, so that the
-  // two column groups of a quarter-warp fall on different banks)
-  float ap[kApReg ? PP : 1][VEC];
+  // ape of this thread's slots, scaled by log2 e: registers (column pairs), or shared memory
+  // as [4-column group][position] float4 (written by group 0; groups W + 4 apart, so that
+  // the two column groups of a quarter-warp fall on different banks)
+  uint64_t ap[kApReg ? PPG : 1][NW];
   float4* sAp = reinterpret_cast<float4*>(smem + p.ape_off) + (wi * 2 + ch) * (W + 4);
   if (kApReg || grp == 0) {
 #pragma unroll
-    for (int i = 0; i < PP; ++i) {
+    for (int ii = 0; ii < (kApReg ? PPG : PP); ++ii) {
+      const int i = (kApReg && kPS ? grp * PPG : 0) + ii;
       const int w = pg + 16 * i;
       const bool prev = two && w < r;
       const int arow = (two && !prev) ? w - r : w;
@@ -304,10 +354,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       a.z *= kLog2e;
       a.w *= kLog2e;
       if constexpr (kApReg) {
-        ap[i][0] = a.x;
-        ap[i][1] = a.y;
-        ap[i][2] = a.z;
-        ap[i][3] = a.w;
+        ap[ii][0] = f2_pack(a.x, a.y);
+        ap[ii][1] = f2_pack(a.z, a.w);
       } else {
         sAp[w] = a;
       }
@@ -315,117 +363,173 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   }
   if constexpr (!kApReg) asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // ape staged
 
-  // (16 positions per lane: the shared-memory reads are volatile, so that the compiler does
-  // not hoist all positions' reads ahead and run out of registers)
-  auto ape_at = [&](const int i, const int w) -> float4 {
+  // ape' of the lane's position index ii (window position w) as two column pairs. (16
+  // positions per lane: the shared-memory reads are volatile, so that the compiler does not
+  // hoist all positions' reads ahead and run out of registers.)
+  auto ape_at = [&](const int ii, const int w, uint64_t (&a2)[NW]) {
     if constexpr (kApReg) {
-      return make_float4(ap[i][0], ap[i][1], ap[i][2], ap[i][3]);
-    } else if constexpr (PP >= 16) {
-      const uint4 t = lds128_fresh(sAp + w);
-      return make_float4(__uint_as_float(t.x), __uint_as_float(t.y), __uint_as_float(t.z),
-                         __uint_as_float(t.w));
+      a2[0] = ap[ii][0];
+      a2[1] = ap[ii][1];
     } else {
-      return sAp[w];
+      uint4 t;
+      if constexpr (PP >= 16) {
+        t = lds128_fresh(sAp + w);
+      } else {
+        const float4 f = sAp[w];
+        t = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z),
+                       __float_as_uint(f.w));
+      }
+      a2[0] = (static_cast<uint64_t>(t.y) << 32) | t.x;
+      a2[1] = (static_cast<uint64_t>(t.w) << 32) | t.z;
     }
   };
 
-  float acc[BWD ? PP : 1][VEC];  // backward dAPE sums of this thread's slots
+  uint64_t acc[BWD ? PPG : 1][NW];  // backward dAPE sums of this thread's slots (column pairs)
+  const int ib = kPS ? grp * PPG : 0;  // this group's first position index (pg + 16 ib)
+  // the position split's exchange of the groups' column max and sums (just below the ring)
+  float (*s_xm)[kLongSlice] = reinterpret_cast<float (*)[kLongSlice]>(
+      smem + p.ring_off - (kPS ? 3 * 2 * kLongSlice * 4 : 0));
+  float (*s_xz)[kLongSlice] = s_xm + 2;
+  float (*s_xa)[kLongSlice] = s_xm + 4;
 #pragma unroll
-  for (int i = 0; i < (BWD ? PP : 1); ++i)
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) acc[i][c] = 0.f;
+  for (int i = 0; i < (BWD ? PPG : 1); ++i) acc[i][0] = acc[i][1] = 0ull;
+  const uint64_t kL2 = f2_pack(kLog2e, kLog2e);
+  // With packed arithmetic (kPk) the column max takes two positions per instruction where a
+  // pair of position indices
+  // (ii even) is valid or invalid as a whole: positions pg + 16 i are in the previous half
+  // exactly when i < ratio / 16, an even number unless the window has 32 positions over two
+  // halves (with one half of 8 positions the split even depends on the lane).
+  constexpr int kStep = (kPk && PPG >= 2 && !(COFF == 2 && PP <= 2)) ? 2 : 1;
 
   // this thread's tile offset for position pg + 16 i is sw0 + 2048 i: the swizzle depends on
   // the tile row only through its low three bits, which are those of pg
   const int sw0 = swz(pg, wi) + ch * 8;
-  int s = nrows > grp ? find_segment(sB, p.S, o0 + grp) : 0;
-  // stage of row j and its lap (j / depth) % 4, advanced by NG rows per iteration (NG <
-  // depth): the new slot is below NG exactly when it wrapped
-  int slot = grp;
+  const int j0 = kPS ? 0 : grp;
+  int s = nrows > j0 ? find_segment(sB, p.S, o0 + j0) : 0;
+  // stage of row j and its lap (j / depth) % 4, advanced by RSTEP rows per iteration (RSTEP
+  // < depth): the new slot is below RSTEP exactly when it wrapped
+  int slot = j0;
   uint32_t lap = 0;
-  for (int j = grp; j < nrows; j += NG,
-           slot = slot + NG >= p.depth ? slot + NG - p.depth : slot + NG,
-           lap = (lap + (slot < NG)) & 3u) {
+  for (int j = j0; j < nrows; j += RSTEP,
+           slot = slot + RSTEP >= p.depth ? slot + RSTEP - p.depth : slot + RSTEP,
+           lap = (lap + (slot < RSTEP)) & 3u) {
     const int o = o0 + j;
     s = advance_segment(sB, s, o);
     const int b = o - sB[s];
-    const int base = sCu[s] + b * r;
     const bool has_prev = two && b >= 1;
     const bool ok =
         mbar_wait_bounded(&full[slot + ((lap & 1u) ? p.depth : 0)], lap >> 1, p.wait_cycles);
-    if (!__all_sync(0xFFFFFFFFu, ok)) {  // a copy wait ran out: stop, and say so
-      stop_and_drain();
-      break;
+    if constexpr (kPS) {
+      // both groups work on this row and meet at its exchanges: they decide together
+      if (!ok) stop_and_drain();
+      if (!bar_and(2, NCT, ok && *reinterpret_cast<volatile int*>(&s_abort) == 0)) break;
+    } else {
+      if (!__all_sync(0xFFFFFFFFu, ok)) {  // a copy wait ran out: stop, and say so
+        stop_and_drain();
+        break;
+      }
+      if (__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s_abort) != 0)) break;
     }
-    if (__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s_abort) != 0)) break;
     unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
 
-    // x' = score*log2e + ape' at this thread's slots; invalid (first block, previous half)
-    // slots are skipped. With kRecomp the later passes read the slots again instead of
-    // keeping x' (and e) in registers.
-    auto x_at = [&](const int i, const int w, float (&x)[VEC]) {
+    // x' = score*log2e + ape' at this thread's slots, as two column pairs; invalid (first
+    // block, previous half) slots are skipped. With kRecomp the later passes read the slots
+    // again instead of keeping x' (and e) in registers.
+    auto x_at = [&](const int ii, const int i, const int w, uint64_t (&x)[NW]) {
       uint32_t sw[NW];
       if constexpr (PP >= 16) lds_words_fresh<NW>(sw, st + kTile + sw0 + i * 2048);
       else lds_words<NW>(sw, st + kTile + sw0 + i * 2048);
-      const float4 a4 = ape_at(i, w);
-      x[0] = fmaf(bf16_lo(sw[0]), kLog2e, a4.x);
-      x[1] = fmaf(bf16_hi(sw[0]), kLog2e, a4.y);
-      x[2] = fmaf(bf16_lo(sw[1]), kLog2e, a4.z);
-      x[3] = fmaf(bf16_hi(sw[1]), kLog2e, a4.w);
+      uint64_t a2[NW];
+      ape_at(ii, w, a2);
+#pragma unroll
+      for (int q = 0; q < NW; ++q) x[q] = c2_fma<kPk>(bf2_to_f2(sw[q]), kL2, a2[q]);
     };
-    float e[kRecomp ? 1 : PP][VEC];
+    uint64_t e[kRecomp ? 1 : PPG][NW];
     float m[VEC] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int i = 0; i < PP; ++i) {
+    for (int ii = 0; ii < PPG; ii += kStep) {
+      const int i = ib + ii;
       const int w = pg + 16 * i;
       if (two && w < r && !has_prev) continue;
-      float x[VEC];
-      x_at(i, w, x);
+      uint64_t x[kStep][NW];
 #pragma unroll
-      for (int c = 0; c < VEC; ++c) {
-        if constexpr (!kRecomp) e[i][c] = x[c];
-        m[c] = fmaxf(m[c], x[c]);
+      for (int h = 0; h < kStep; ++h) {
+        x_at(ii + h, i + h, w + 16 * h, x[h]);
+        if constexpr (!kRecomp) {
+          e[ii + h][0] = x[h][0];
+          e[ii + h][1] = x[h][1];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NW; ++q) {
+        if constexpr (kStep == 2) {
+          m[2 * q] = fmax3(m[2 * q], f2_lo(x[0][q]), f2_lo(x[1][q]));
+          m[2 * q + 1] = fmax3(m[2 * q + 1], f2_hi(x[0][q]), f2_hi(x[1][q]));
+        } else {
+          m[2 * q] = fmaxf(m[2 * q], f2_lo(x[0][q]));
+          m[2 * q + 1] = fmaxf(m[2 * q + 1], f2_hi(x[0][q]));
+        }
       }
     }
 #pragma unroll
     for (int k = 2; k < 32; k <<= 1)
 #pragma unroll
       for (int c = 0; c < VEC; ++c) m[c] = fmaxf(m[c], __shfl_xor_sync(0xFFFFFFFFu, m[c], k));
+    if constexpr (kPS) {  // the column max over both halves (exact: the same in both groups)
+      if (pg == 0)
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) s_xm[grp][cl + c] = m[c];
+      asm volatile("bar.sync 2, %0;" ::"n"(NCT) : "memory");
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) m[c] = fmaxf(m[c], s_xm[grp ^ 1][cl + c]);
+    }
+    const uint64_t nm[NW] = {f2_pack(-m[0], -m[1]), f2_pack(-m[2], -m[3])};
+    // e = 2^(x' - m) of a slot's column pairs
+    auto exp_at = [&](const uint64_t (&x)[NW], uint64_t (&ec)[NW]) {
+#pragma unroll
+      for (int q = 0; q < NW; ++q) {
+        const uint64_t dd = c2_add<kPk>(x[q], nm[q]);
+        ec[q] = f2_pack(fast_exp2(f2_lo(dd)), fast_exp2(f2_hi(dd)));
+      }
+    };
 
-    // e = 2^(x' - m); two accumulation chains per column (one in the backward, which is
-    // short of registers)
+    // two accumulation chains per column (one in the backward, which is short of registers)
     constexpr int NCH = BWD ? 1 : 2;
-    float z[2][VEC], a[2][VEC];
+    uint64_t z[2][NW], a[2][NW];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) z[0][c] = z[1][c] = a[0][c] = a[1][c] = 0.f;
+    for (int q = 0; q < NW; ++q) z[0][q] = z[1][q] = a[0][q] = a[1][q] = 0ull;
 #pragma unroll
-    for (int i = 0; i < PP; ++i) {
+    for (int ii = 0; ii < PPG; ++ii) {
+      const int i = ib + ii;
       const int w = pg + 16 * i;
       if (two && w < r && !has_prev) continue;
       uint32_t kw[NW];
       if constexpr (PP >= 16) lds_words_fresh<NW>(kw, st + sw0 + i * 2048);
       else lds_words<NW>(kw, st + sw0 + i * 2048);
-      const float v[VEC] = {bf16_lo(kw[0]), bf16_hi(kw[0]), bf16_lo(kw[1]), bf16_hi(kw[1])};
-      float x[VEC];
+      uint64_t x[NW], ec[NW];
       if constexpr (kRecomp) {
-        x_at(i, w, x);
+        x_at(ii, i, w, x);
       } else {
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) x[c] = e[i][c];
+        x[0] = e[ii][0];
+        x[1] = e[ii][1];
       }
+      exp_at(x, ec);
 #pragma unroll
-      for (int c = 0; c < VEC; ++c) {
-        const float ec = fast_exp2(x[c] - m[c]);
-        if constexpr (!kRecomp) e[i][c] = ec;
-        z[i % NCH][c] += ec;
-        a[i % NCH][c] = fmaf(ec, v[c], a[i % NCH][c]);
+      for (int q = 0; q < NW; ++q) {
+        if constexpr (!kRecomp) e[ii][q] = ec[q];
+        z[ii % NCH][q] = c2_add<kPk>(z[ii % NCH][q], ec[q]);
+        a[ii % NCH][q] = c2_fma<kPk>(ec[q], bf2_to_f2(kw[q]), a[ii % NCH][q]);
       }
     }
     float Z[VEC], A[VEC];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) {
-      Z[c] = z[0][c] + z[1][c];
-      A[c] = a[0][c] + a[1][c];
+    for (int q = 0; q < NW; ++q) {
+      const uint64_t zq = c2_add<kPk>(z[0][q], z[1][q]);
+      const uint64_t aq = c2_add<kPk>(a[0][q], a[1][q]);
+      Z[2 * q] = f2_lo(zq);
+      Z[2 * q + 1] = f2_hi(zq);
+      A[2 * q] = f2_lo(aq);
+      A[2 * q + 1] = f2_hi(aq);
     }
 #pragma unroll
     for (int k = 2; k < 32; k <<= 1)
@@ -434,6 +538,20 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         Z[c] += __shfl_xor_sync(0xFFFFFFFFu, Z[c], k);
         A[c] += __shfl_xor_sync(0xFFFFFFFFu, A[c], k);
       }
+    if constexpr (kPS) {  // both halves' sums, added in group order: the same bits in both
+      if (pg == 0)
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          s_xz[grp][cl + c] = Z[c];
+          s_xa[grp][cl + c] = A[c];
+        }
+      asm volatile("bar.sync 2, %0;" ::"n"(NCT) : "memory");
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        Z[c] = s_xz[0][cl + c] + s_xz[1][cl + c];
+        A[c] = s_xa[0][cl + c] + s_xa[1][cl + c];
+      }
+    }
     float rz[VEC], oc[VEC];
 #pragma unroll
     for (int c = 0; c < VEC; ++c) {
@@ -441,46 +559,43 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       oc[c] = A[c] * rz[c];
     }
     if constexpr (!BWD) {
-      if (pg == 0) {
+      if (pg == 0 && (!kPS || grp == 0)) {
         uint32_t ow[NW] = {pack_bf16x2(oc[0], oc[1]), pack_bf16x2(oc[2], oc[3])};
         store_stream<NW>(p.out + static_cast<int64_t>(o) * d + col0 + cl, ow);
       }
     } else {
       uint32_t gw[NW];
       lds_words<NW>(gw, gring + slot * kLongSlice * 2 + cl * 2);
-      const float gv[VEC] = {bf16_lo(gw[0]), bf16_hi(gw[0]), bf16_lo(gw[1]), bf16_hi(gw[1])};
-      float qg[VEC];
+      const uint64_t qg[NW] = {f2_pack(rz[0] * bf16_lo(gw[0]), rz[1] * bf16_hi(gw[0])),
+                               f2_pack(rz[2] * bf16_lo(gw[1]), rz[3] * bf16_hi(gw[1]))};
+      const uint64_t noc[NW] = {f2_pack(-oc[0], -oc[1]), f2_pack(-oc[2], -oc[3])};
 #pragma unroll
-      for (int c = 0; c < VEC; ++c) qg[c] = rz[c] * gv[c];
-#pragma unroll
-      for (int i = 0; i < PP; ++i) {
+      for (int ii = 0; ii < PPG; ++ii) {
+        const int i = ib + ii;
         const int w = pg + 16 * i;
         const bool prev = two && w < r;
         if (prev && !has_prev) continue;
         uint32_t kw[NW];
         lds_words_fresh<NW>(kw, st + sw0 + i * 2048);
-        const float v[VEC] = {bf16_lo(kw[0]), bf16_hi(kw[0]), bf16_lo(kw[1]), bf16_hi(kw[1])};
-        float ei[VEC];
+        uint64_t ei[NW];
         if constexpr (kRecomp) {
-          float x[VEC];
-          x_at(i, w, x);
-#pragma unroll
-          for (int c = 0; c < VEC; ++c) ei[c] = fast_exp2(x[c] - m[c]);
+          uint64_t x[NW];
+          x_at(ii, i, w, x);
+          exp_at(x, ei);
         } else {
-#pragma unroll
-          for (int c = 0; c < VEC; ++c) ei[c] = e[i][c];
+          ei[0] = e[ii][0];
+          ei[1] = e[ii][1];
         }
-        float kk[VEC], t[VEC];
+        uint64_t kk[NW], t[NW];
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-          kk[c] = ei[c] * qg[c];
-          t[c] = kk[c] * (v[c] - oc[c]);
-          acc[i][c] += t[c];
+        for (int q = 0; q < NW; ++q) {
+          kk[q] = c2_mul<kPk>(ei[q], qg[q]);
+          t[q] = c2_mul<kPk>(kk[q], c2_add<kPk>(bf2_to_f2(kw[q]), noc[q]));
+          acc[ii][q] = c2_add<kPk>(acc[ii][q], t[q]);
         }
         // dKV and dScore replace the kv and score values of this slot in the stage
-        sts_words2(st + sw0 + i * 2048, pack_bf16x2(kk[0], kk[1]), pack_bf16x2(kk[2], kk[3]));
-        sts_words2(st + kTile + sw0 + i * 2048, pack_bf16x2(t[0], t[1]),
-                   pack_bf16x2(t[2], t[3]));
+        sts_words2(st + sw0 + i * 2048, f2_to_bf2(kk[0]), f2_to_bf2(kk[1]));
+        sts_words2(st + kTile + sw0 + i * 2048, f2_to_bf2(t[0]), f2_to_bf2(t[1]));
       }
       // (the zeros owned by a segment's last block are written by the zero warp)
     }
@@ -493,33 +608,33 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   }
 
   if constexpr (BWD) {
-    // the CTA's dAPE partial for this thread's slots: group 0's sums, then group 1's
-    if constexpr (NG == 2) {
+    // the CTA's dAPE partial for this thread's slots: group 0's sums, then group 1's (with
+    // the position split each group owns its positions' slots)
+    if constexpr (NG == 2 && !kPS) {
       asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // ape no longer read
       if (grp == 1)
 #pragma unroll
         for (int i = 0; i < PP; ++i)
-          sAp[pg + 16 * i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+          sAp[pg + 16 * i] = make_float4(f2_lo(acc[i][0]), f2_hi(acc[i][0]), f2_lo(acc[i][1]),
+                                         f2_hi(acc[i][1]));
       asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
       if (grp == 1) return;
 #pragma unroll
       for (int i = 0; i < PP; ++i) {
         const float4 o1v = sAp[pg + 16 * i];
-        acc[i][0] += o1v.x;
-        acc[i][1] += o1v.y;
-        acc[i][2] += o1v.z;
-        acc[i][3] += o1v.w;
+        acc[i][0] = c2_add<kPk>(acc[i][0], f2_pack(o1v.x, o1v.y));
+        acc[i][1] = c2_add<kPk>(acc[i][1], f2_pack(o1v.z, o1v.w));
       }
     }
     float* dst = p.partial + static_cast<int64_t>(g) * r * C;
 #pragma unroll
-    for (int i = 0; i < PP; ++i) {
-      const int w = pg + 16 * i;
+    for (int ii = 0; ii < PPG; ++ii) {
+      const int w = pg + 16 * (ib + ii);
       const bool prev = two && w < r;
       const int arow = (two && !prev) ? w - r : w;
       const int col = ((two && !prev) ? d : 0) + col0 + cl;
       *reinterpret_cast<float4*>(dst + static_cast<int64_t>(arow) * C + col) =
-          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+          make_float4(f2_lo(acc[ii][0]), f2_hi(acc[ii][0]), f2_lo(acc[ii][1]), f2_hi(acc[ii][1]));
     }
   }
 }

@@ -123,7 +123,7 @@ def small_packs():
 
 
 SMALL = small_packs()
-FULL = ["tiny", "1x8192_d128", "3x8192_d512", "ragged_r2_d512", "long_r128_d512"]
+FULL = ["tiny", "1x8192_d128", "3x8192_d512", "ragged_r2_d512", "long_r128_d512", "r128c2_d128"]
 
 
 def check_fwd(gp, pack, shift=0, label=None):
