@@ -218,10 +218,9 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       if (tid == NCT + 32) {
         int s = nrows > 0 ? find_segment(sB, p.S, o0) : 0;
         bool bad = false;
-        int slot = 0, pslot = 0;  // stages of rows j and j - 1
-        uint32_t ph = 0;          // (j / depth) & 1
-        for (int j = 0; j < nrows;
-             ++j, pslot = slot, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
+        int slot = 0;     // stage of row j
+        uint32_t ph = 0;  // (j / depth) & 1
+        for (int j = 0; j < nrows; ++j, slot = slot + 1 == p.depth ? 0 : slot + 1, ph ^= slot == 0) {
           if (!mbar_wait_bounded(&done[slot], ph, p.wait_cycles) ||
               *reinterpret_cast<volatile int*>(&s_abort)) {
             bad = true;
@@ -240,10 +239,11 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
           tma_store_2d(&tm_dkv, x, base, st + yo);
           tma_store_2d(&tm_dsc, x, base, st + kTile + yo);
           bulk_commit();
-          if (j >= 1) {  // the previous row's tiles have been read: hand its stage back
-            bulk_wait_read<1>();
-            mbar_arrive(&empty[pslot]);
-          }
+          // hand the stage back as soon as its tiles have been read (the next row's
+          // gradients are still being computed: nothing else waits for this warp), so that
+          // the producer refills it while the consumers work on the next row
+          bulk_wait_read<0>();
+          mbar_arrive(&empty[slot]);
         }
         bulk_wait_all();
         if (bad) stop_and_drain();
