@@ -116,9 +116,10 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 matrix [rows, cols] (row stride cols), boxes of [box_rows, box_cols] written to
-// shared memory with the 128-byte swizzle (box_cols * 2 must be 128).
+// shared memory with the (box_cols * 2)-byte swizzle (box_cols 64 or 32).
 bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int cols, int box_cols,
                      int box_rows) {
+  if (box_cols != 64 && box_cols != 32) return false;
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols),
@@ -127,7 +128,8 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int cols,
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t elem[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -175,7 +177,9 @@ csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t
     if (!plan_generic(bwd, S, ratio, coff, d, limit, pl)) return CSA_ERR_UNSUPPORTED;
   } else if (!(!bwd && plan_fwd_ldg(S, ratio, coff, d, limit, pl)) &&
              !plan_stream(bwd, S, ratio, coff, d, limit, pl) &&
-             !(encode_fn() != nullptr && plan_long(bwd, S, ratio, coff, d, limit, pl))) {
+             !(encode_fn() != nullptr &&
+               plan_long(bwd, S, ratio, coff, d, long_slice_cols(coff * ratio, d, out_rows, sms),
+                         limit, pl))) {
     *pl = plan_shape(bwd, S, ratio, coff, d);
   }
   *kernel = bwd ? bwd_kernel_for(*pl) : fwd_kernel_for(*pl);
@@ -184,7 +188,11 @@ csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t
       cudaSuccess)
     return CSA_ERR_CUDA;
   if (bps < 1) return CSA_ERR_UNSUPPORTED;  // shared memory of the plan does not fit
-  int64_t want = (static_cast<int64_t>(sms) * bps + pl->K - 1) / pl->K;
+  // row groups: as many as fill the SMs' resident CTAs once over the K column slices,
+  // rounded down (rounding up would leave the last few CTAs to run in a second wave after
+  // the rest, nearly doubling the time when K does not divide that count)
+  int64_t want = static_cast<int64_t>(sms) * bps / pl->K;
+  if (want < 1) want = 1;
   // the generic kernel's many small CTAs: at most one row group per SM, so that its dAPE
   // partials need no more workspace than the vector kernels'
   if (pl->generic && want > sms) want = sms;
@@ -263,7 +271,7 @@ csa_status_t launch(PoolKernel k, const Plan& pl, PoolParams& p, cudaStream_t st
     // (the backward also stores dKV and dScore through maps; the forward gets copies of
     // the input maps in those places and never uses them)
     CUtensorMap mkv, msc, mdkv, mdsc;
-    const int sw = 4 * pl.Vs;  // 64 columns = one 128-byte swizzle row
+    const int sw = 4 * pl.Vs;  // the slice: 64 (or 32) columns = one 128 (64)-byte swizzle row
     const void* kv = p.kv != nullptr ? static_cast<const void*>(p.kv) : p.ape;
     const void* sc = p.score != nullptr ? static_cast<const void*>(p.score) : p.ape;
     const void* dkv = p.dkv != nullptr ? static_cast<const void*>(p.dkv) : kv;

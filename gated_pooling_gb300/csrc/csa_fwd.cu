@@ -13,17 +13,24 @@ PoolKernel fwd_kernel_for(const Plan& pl) {
   if (pl.longk) {
     const bool two = pl.coff == 2;
     switch (pl.pp) {
-      case 1: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, 2, false>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, 1, false>);
-      case 2: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, 2, false>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, 1, false>);
-      case 4: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 2, false>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 1, false>);
-      case 8: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 2, false>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 1, false>);
-      case 16:  // 256-position windows: ratio 128 at coff 2 only
-        return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<16, long_groups(false, 256), 2, false>)
-                   : nullptr;
+      case 1: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, 2, false, 64>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, 1, false, 64>);
+      case 2: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, 2, false, 64>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, 1, false, 64>);
+      case 4: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 2, false, 64>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 1, false, 64>);
+      case 8: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 2, false, 64>)
+                         : reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 1, false, 64>);
+      case 16:  // 256-position windows (ratio 128 at coff 2, ratio 256 at coff 1)
+        if (pl.sc == 32)
+          return two ? reinterpret_cast<PoolKernel>(
+                           pool_long_kernel<16, long_groups(false, 256, 32), 2, false, 32>)
+                     : reinterpret_cast<PoolKernel>(
+                           pool_long_kernel<16, long_groups(false, 256, 32), 1, false, 32>);
+        return two ? reinterpret_cast<PoolKernel>(
+                         pool_long_kernel<16, long_groups(false, 256, 64), 2, false, 64>)
+                   : reinterpret_cast<PoolKernel>(
+                         pool_long_kernel<16, long_groups(false, 256, 64), 1, false, 64>);
       default: return nullptr;
     }
   }

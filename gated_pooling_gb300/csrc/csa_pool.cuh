@@ -468,6 +468,7 @@ struct Plan {
   bool longk = false;  // long windows through 2-D tensor copies (csa_pool_long.cuh)
   bool generic = false;  // any head dim / alignment, scalar (csa_pool_generic.cuh)
   int box_rows = 0;    // long windows: tokens per tensor box
+  int sc = 64;         // long windows: columns per CTA slice (64, or 32)
   int coff = 0;
   int threads = kThreads;
   int np = 1;  // block-streaming kernel: producer warps that stream rows
@@ -658,14 +659,15 @@ inline bool plan_fwd_ldg(int S, int r, int coff, int d, size_t smem_limit, Plan*
 }
 
 // Long-window geometry (csa_pool_long.cuh): W = coff*ratio in {16, 32, 64, 128, 256} and d
-// a multiple of 64. A CTA slice is 64 columns per half (16 chunks of 4); a stage holds the
-// [W x 64] kv and score tiles (tile rows of 128 bytes, 1024-byte aligned for the 128-byte
-// swizzle; at coff=2 the own half starts at tile row ratio, a multiple of 8), the backward
-// adds the dout slice in a ring of its own. Tensor boxes (loads, and the backward's
-// stores) are [ratio tokens x 64 columns].
+// a multiple of the slice width sc (64 columns per half, 16 chunks of 4; 32 for
+// 256-position windows). A stage holds the [W x sc] kv and score tiles (tile rows of 2·sc
+// bytes, 1024-byte aligned for the 2·sc-byte swizzle; at coff=2 the own half starts at
+// tile row ratio, a multiple of 8), the backward adds the dout slice in a ring of its own.
+// Tensor boxes (loads, and the backward's stores) are [ratio tokens x sc columns].
 constexpr int kLongSliceCols = 64;  // columns per half in a long-window CTA slice
 
-// Consumer groups of 8 warps in the long-window kernel (csa_pool_long.cuh), per direction.
+// Consumer groups of 8 warps in the long-window kernel (csa_pool_long.cuh) on 64-column
+// slices, per direction.
 #ifndef CSA_LONG_FWD_GROUPS
 #define CSA_LONG_FWD_GROUPS 3
 #endif
@@ -673,30 +675,59 @@ constexpr int kLongSliceCols = 64;  // columns per half in a long-window CTA sli
 #define CSA_LONG_BWD_GROUPS 2
 #endif
 
-// Consumer groups of the long-window kernel for a window of W positions. 256-position
-// windows (ratio 128 at coff 2) have 64 KB stages, of which only two or three fit, so two
+// Columns per CTA slice of the long-window kernel: 64, or 32 for a 256-position window
+// whose head dim is not a multiple of 64 or whose 64-column slices would give the SMs fewer
+// than 16 rows each (the pages' 65k-token r128 coff 2 d128 example: 512 rows of 64 KB per
+// slice, 6.7 per SM). Narrower slices give each CTA twice the rows, half as large, so that
+// the pipeline's fill and drain weigh less: that example's step 60.7 -> 53.2 us; with 27
+// rows per SM (d512) the 64-column slices stay 2% faster. (CSA_LONG_W256_SC = 32 or 64
+// forces one width.)
+#ifndef CSA_LONG_W256_SC
+#define CSA_LONG_W256_SC 0
+#endif
+inline int long_slice_cols(int W, int d, int64_t out_rows, int sms) {
+  if (W < 256) return kLongSliceCols;
+  if (CSA_LONG_W256_SC != 0) return CSA_LONG_W256_SC;
+  if (d % 64 != 0) return 32;
+  const int64_t rows_per_sm = out_rows * (d / 64) / (sms > 0 ? sms : 1);
+  return rows_per_sm < 16 ? 32 : kLongSliceCols;
+}
+
+// Consumer groups of the long-window kernel for a window of W positions. On 64-column
+// slices a 256-position window has 64 KB stages, of which only two or three fit, so two
 // groups do not take alternate rows there: both take every row, each half of its positions
-// (the position split). The backward runs it (r128c2 d128: 57.6 -> 54.4 us); the forward
-// measured slower with it (20.5 -> 21.1 us) and runs one group.
+// (the position split), which the backward runs (r128c2 d128: 57.6 -> 54.4 us; the forward
+// measured slower with it, 20.5 -> 21.1 us, and runs one group). On 32-column slices the
+// groups have 4 warps and take alternate rows.
 #ifndef CSA_LONG_W256_FWD_GROUPS
 #define CSA_LONG_W256_FWD_GROUPS 1
 #endif
 #ifndef CSA_LONG_W256_BWD_GROUPS
 #define CSA_LONG_W256_BWD_GROUPS 2
 #endif
-constexpr int long_groups(bool bwd, int W) {
-  return W >= 256 ? (bwd ? CSA_LONG_W256_BWD_GROUPS : CSA_LONG_W256_FWD_GROUPS)
+constexpr int long_groups(bool bwd, int W, int sc) {
+  return W >= 256 ? (sc == 32 ? 2 : (bwd ? CSA_LONG_W256_BWD_GROUPS : CSA_LONG_W256_FWD_GROUPS))
                   : (bwd ? CSA_LONG_BWD_GROUPS : CSA_LONG_FWD_GROUPS);
+}
+// The position split: two groups on a 64-column slice of a 256-position window.
+constexpr bool long_position_split(int W, int ng, int sc) {
+  return ng == 2 && W >= 256 && sc == 64;
+}
+// The forward keeps a lane's ape in registers where its consumers have 8 warps (registers
+// for 168 a thread) or split the positions; otherwise ape sits in shared memory.
+constexpr bool long_ape_in_regs(bool bwd, int W, int ng, int sc) {
+  return !bwd && (ng * sc * 4 <= 256 || long_position_split(W, ng, sc));
 }
 
 #ifndef CSA_LONG_W256
 #define CSA_LONG_W256 1  // 256-position windows on the long-window kernel (else the split kernel)
 #endif
-inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit, Plan* out) {
+// sc: columns per slice (long_slice_cols).
+inline bool plan_long(bool bwd, int S, int r, int coff, int d, int sc, size_t smem_limit,
+                      Plan* out) {
   const int W = coff * r;
-  if (!(W == 16 || W == 32 || W == 64 || W == 128 || (CSA_LONG_W256 && W == 256)) ||
-      d % 64 != 0)
-    return false;
+  if (!(W == 16 || W == 32 || W == 64 || W == 128 || (CSA_LONG_W256 && W == 256))) return false;
+  if ((sc != 64 && sc != 32) || (sc == 32 && W != 256) || d % sc != 0) return false;
   Plan pl;
   pl.longk = true;
   pl.coff = coff;
@@ -704,29 +735,30 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, size_t smem_limit
   pl.pp = W / 16;
   pl.P = 16;
   pl.V = d / 4;
-  pl.Vs = 16;
-  pl.K = d / 64;
+  pl.Vs = sc / 4;
+  pl.K = d / sc;
+  pl.sc = sc;
   pl.slots = 1;
   pl.box_rows = r;
   pl.sB_words = ((S + 1) + 3) & ~3;
-  const int ng = long_groups(bwd, W);
-  // the forward keeps ape in registers with one group, or with a 256-position window
-  const bool ape_smem = bwd || (ng > 1 && W < 256);
+  const int ng = long_groups(bwd, W, sc);
+  const bool ape_smem = !long_ape_in_regs(bwd, W, ng, sc);
   const size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
-  // the position split's column max and sums exchange ([3][2 groups][64 columns] floats)
+  // the position split's column max and sums exchange ([3][2 groups][sc columns] floats)
   // sits just below the ring
-  const size_t xch = (W >= 256 && ng == 2) ? (size_t)3 * 2 * kLongSliceCols * 4 : 0;
-  const size_t ring_off = ape_off + (ape_smem ? (size_t)16 * (W + 4) * 16 : 0) + xch;
-  pl.stage_bytes = 2 * W * 128;
+  const size_t xch = long_position_split(W, ng, sc) ? (size_t)3 * 2 * sc * 4 : 0;
+  const size_t ring_off =
+      ape_off + (ape_smem ? (size_t)(sc / 4) * (W + 4) * 16 : 0) + xch;
+  pl.stage_bytes = 2 * W * sc * 2;
   // + the dout slice and 4 mbarriers (backward: two full, empty, done), 3 (forward)
-  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? 128 + 32 : 24);
+  const size_t per_stage = (size_t)pl.stage_bytes + (bwd ? (size_t)sc * 2 + 32 : 24);
   if (smem_limit < ring_off + 1024 + 2 * per_stage) return false;
   const size_t depth = std::min<size_t>(16, (smem_limit - ring_off - 1024) / per_stage);
-  // every consumer group needs a stage of its own (the groups of a 256-position window
-  // share theirs)
-  if (depth <= (size_t)(W >= 256 ? 1 : ng)) return false;
+  // every consumer group needs a stage of its own (the groups of the position split share
+  // theirs)
+  if (depth <= (size_t)(long_position_split(W, ng, sc) ? 1 : ng)) return false;
   pl.depth = (int)depth;
-  pl.threads = ng * kThreads + (bwd ? 96 : 32);  // + producer warp (+ store and zero warps)
+  pl.threads = ng * sc * 4 + (bwd ? 96 : 32);  // + producer warp (+ store and zero warps)
   pl.ape_off = (int)ape_off;
   pl.ring_off = (int)ring_off;
   pl.smem = ring_off + 1024 + depth * per_stage;

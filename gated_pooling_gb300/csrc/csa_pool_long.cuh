@@ -1,29 +1,31 @@
 // csa_pool_long.cuh -- pooling kernel for long windows (W = coff*ratio in {16, 32, 64, 128,
 // 256}; e.g. the ratio=128 family of "Megatron-LM PR #5984", commit "add dedicated
 // ratio=128 kernels", at coff 1 and 2), forward and backward, for head dims that are
-// multiples of 64.
+// multiples of the slice width (64 columns; 32 for 256-position windows).
 //
-// Same operation and zero ownership as pool_kernel (csa_pool.cuh). A CTA owns a slice of 64
-// columns per half and a contiguous range of output rows. For each row a producer warp
-// loads the slice's window with 2-D tensor-map bulk copies (TMA, 128-byte swizzle): one box
-// of [ratio tokens x 64 columns] per tensor per block half (at coff=2 the previous block at
+// Same operation and zero ownership as pool_kernel (csa_pool.cuh). A CTA owns a slice of SC
+// columns per half (64, or 32 for 256-position windows, whose rows are few: narrower slices
+// give each CTA twice the rows, half as large) and a contiguous range of output rows. For
+// each row a producer warp loads the slice's window with 2-D tensor-map bulk copies (TMA,
+// 2·SC-byte swizzle): one box of [ratio tokens x SC columns] per tensor per block half (at
+// coff=2 the previous block at
 // the slice's first-half columns, the own block at its second-half columns), plus the dout
 // slice in the backward, into a ring of shared-memory stages completing on mbarriers. The
 // backward writes each slot's dKV and dScore over the kv and score values it has consumed in
 // the stage (every slot has exactly one reader and writer), and a store warp copies the
-// finished tiles out with tensor-map bulk stores, whole 128-byte tile rows at a time, before
-// it hands the stage back to the producer. A zero warp writes meanwhile the zeros of short
+// finished tiles out with tensor-map bulk stores, whole tile rows at a time, and hands the
+// stage back to the producer as soon as they have been read out. A zero warp writes meanwhile the zeros of short
 // segments, of the rows outside [cu[0], cu[S]), and of the segments whose last block is a
 // row of the CTA (that block's own first-half columns at coff=2, and the segment's tail).
 //
-// Consumers are NG groups of 8 warps; group h takes the rows h, h+NG, ... of the CTA's
+// Consumers are NG groups of SC/8 warps; group h takes the rows h, h+NG, ... of the CTA's
 // range (more groups keep more warps in flight where registers allow). Warp wi of a
 // group owns the 8 columns [8wi, 8wi+8) of the slice; its lane (pg = lane / 2,
 // ch = lane % 2) owns 4 of them and the window positions pg, pg+16, pg+32, ... A column's
 // max and its sums (sum e, sum e*kv) are reduced over the 16 position lanes with xor
 // shuffles; the adds of a butterfly are commutative, so all 16 lanes end with the same
 // bits and the result is the same on every run. Warps never wait for each other: a stage
-// is released once the 256 threads of its group have arrived on its `empty` barrier. The
+// is released once the threads of its group have arrived on its `empty` barrier. The
 // swizzle puts the 8 rows that each half-warp reads at once on disjoint banks. The ape
 // values of a thread's slots are kept in registers (forward, one group) or in shared
 // memory; in the backward the registers hold the thread's dAPE sums, which the groups add
@@ -38,7 +40,6 @@
 
 namespace csa {
 
-constexpr int kLongSlice = kLongSliceCols;  // one 128-byte tile row
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar, uint64_t policy) {
@@ -74,9 +75,15 @@ __device__ __forceinline__ void sts_words2(void* p, uint32_t a, uint32_t b) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_addr(p)), "r"(a), "r"(b) : "memory");
 }
 
-// Byte offset of (tile row y, 16-byte chunk c) in a tile of 128-byte rows written with the
-// 128-byte swizzle (tile base on a 1024-byte boundary): the chunk is stored at c ^ (y mod 8).
-__device__ __forceinline__ int swz(int y, int c) { return y * 128 + ((c ^ (y & 7)) << 4); }
+// Byte offset of (tile row y, 16-byte chunk c) in a tile of SC-column rows written with the
+// 2·SC-byte swizzle (tile base on a 1024-byte boundary): 128-byte rows keep chunk c at
+// c ^ (y mod 8), 64-byte rows at c ^ ((y / 2) mod 4) (the swizzle XORs address bits 4-6,
+// resp. 4-5, with bits 7-9, resp. 7-8).
+template <int SC>
+__device__ __forceinline__ int swz(int y, int c) {
+  if constexpr (SC == 64) return y * 128 + ((c ^ (y & 7)) << 4);
+  return y * 64 + ((c ^ ((y >> 1) & 3)) << 4);
+}
 
 // Named barrier `id` over n threads that also ANDs a predicate over them: every thread
 // gets the same answer.
@@ -112,28 +119,33 @@ __device__ __forceinline__ uint64_t c2_mul(uint64_t a, uint64_t b) {
   return f2_pack(f2_lo(a) * f2_lo(b), f2_hi(a) * f2_hi(b));
 }
 
-template <int PP, int NG, int COFF, bool BWD>
-__global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
+template <int PP, int NG, int COFF, bool BWD, int SC>
+__global__ void __launch_bounds__(NG * SC * 4 + (BWD ? 96 : 32), 1)
     pool_long_kernel(const PoolParams p, const __grid_constant__ CUtensorMap tm_kv,
                      const __grid_constant__ CUtensorMap tm_sc,
                      const __grid_constant__ CUtensorMap tm_dkv,
                      const __grid_constant__ CUtensorMap tm_dsc) {
   constexpr int VEC = 4, NW = 2;
-  constexpr int W = 16 * PP;          // window positions
-  constexpr int kTile = W * 128;      // one tensor's window in a stage
-  constexpr int NCT = NG * kThreads;  // consumer threads
+  static_assert(SC == 64 || SC == 32, "slices of 64 or 32 columns");
+  constexpr int W = 16 * PP;      // window positions
+  constexpr int RB = SC * 2;      // bytes of a tile row (one token of the slice)
+  constexpr int kTile = W * RB;   // one tensor's window in a stage
+  constexpr int kPos = 16 * RB;   // tile bytes between a lane's positions pg + 16 i
+  constexpr int GT = SC * 4;      // threads of a consumer group (SC / 8 warps)
+  constexpr int NCT = NG * GT;    // consumer threads
   static_assert(NG >= 1 && (!BWD || NG <= 2), "the dAPE combine handles two groups");
-  // 256-position windows with two groups: both groups take every row, group g the
-  // positions [128 g, 128 g + 128) (the previous block, then the own block), and they merge
-  // the column max and the sums through shared memory; other windows: the groups take
-  // alternate rows
-  constexpr bool kPS = NG == 2 && PP >= 16;
+  // the position split (two groups on a 64-column slice of a 256-position window): both
+  // groups take every row, group g the positions [128 g, 128 g + 128) (the previous block,
+  // then the own block), and they merge the column max and the sums through shared memory;
+  // otherwise the groups take alternate rows
+  constexpr bool kPS = long_position_split(W, NG, SC);
   constexpr int PPG = kPS ? PP / 2 : PP;  // positions per lane in a row
   constexpr int RSTEP = kPS ? 1 : NG;     // rows a group advances per iteration
-  constexpr bool kApReg = !BWD && (NG == 1 || kPS);  // forward: a lane's ape in registers
+  constexpr bool kApReg = long_ape_in_regs(BWD, W, NG, SC);  // a lane's ape in registers
   // packed f32x2 arithmetic where it measured faster: the forward of 256-position windows,
-  // whose single group of 8 warps is bound by instruction issue (r128c2 d128 forward 20.5
-  // -> 18.1 us); elsewhere it measured slower (up to +15 % for 64-position backwards)
+  // whose 8 consumer warps are bound by instruction issue (r128c2 d128 forward 20.5 -> 18.1
+  // us on 64-column slices); elsewhere it measured slower (up to +15 % for 64-position
+  // backwards)
 #ifndef CSA_LONG_PACKED
 #define CSA_LONG_PACKED 1  // 0: never, 1: 256-position forwards, 2: every instantiation
 #endif
@@ -157,7 +169,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   // row j - depth was armed, which waited until slot j - 2 depth was handed back; that row
   // has landed, so a phase-parity wait on full[j mod 2 depth] is exact (with depth
   // barriers, a slow copy of row j - depth would alias row j's phase)
-  uint64_t* full = reinterpret_cast<uint64_t*>(gring + (BWD ? p.depth * kLongSlice * 2 : 0));
+  uint64_t* full = reinterpret_cast<uint64_t*>(gring + (BWD ? p.depth * SC * 2 : 0));
   uint64_t* empty = full + 2 * p.depth;
   uint64_t* done = empty + p.depth;  // backward: a group has written the stage's gradients
 
@@ -170,8 +182,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     for (int t = tid; t < nb; t += blockDim.x) {
       const int k = t / p.depth;
       if (k < 2) mbar_init(&full[t], 1);
-      else if (k == 2) mbar_init(&empty[t - 2 * p.depth], BWD ? 1 : (kPS ? NCT : kThreads));
-      else mbar_init(&done[t - 3 * p.depth], kPS ? NCT : kThreads);  // (bwd empty: store warp)
+      else if (k == 2) mbar_init(&empty[t - 2 * p.depth], BWD ? 1 : (kPS ? NCT : GT));
+      else mbar_init(&done[t - 3 * p.depth], kPS ? NCT : GT);  // (bwd empty: store warp)
       fence_proxy_async_smem();
     }
     if (tid == 0) {
@@ -189,7 +201,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
 
   const int r = p.r, d = p.d, C = p.C;
   constexpr bool two = COFF == 2;
-  const int col0 = blockIdx.x * kLongSlice;  // first column of the slice (in a half)
+  const int col0 = blockIdx.x * SC;  // first column of the slice (in a half)
   const int g = blockIdx.y;
   const int o0 = static_cast<int>(static_cast<int64_t>(g) * TC / p.R);
   const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
@@ -234,7 +246,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
             tma_store_2d(&tm_dkv, col0, base - r, st);
             tma_store_2d(&tm_dsc, col0, base - r, st + kTile);
           }
-          const int yo = two ? r * 128 : 0;
+          const int yo = two ? r * RB : 0;
           const int x = (two ? d : 0) + col0;
           tma_store_2d(&tm_dkv, x, base, st + yo);
           tma_store_2d(&tm_dsc, x, base, st + kTile + yo);
@@ -257,7 +269,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
       for (int s = s_lo; s < s_hi; ++s) {
         const int a = sCu[s], b = sCu[s + 1];
-        if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, kLongSlice / VEC, zt, 32);
+        if (b - a < r && b > a) zero_rows<NW>(p, a, b - a, SC / VEC, zt, 32);
       }
       // segments whose last block is a row of this group (sB[s+1] - 1 in [o0, o1)): the
       // first-half columns of that block's own tokens (coff=2; no next block reads them)
@@ -269,8 +281,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         const int n = sB[t] - sB[s];
         if (n < 1) continue;
         const int cs = sCu[s], ce = sCu[t];
-        if (two) zero_rows<NW>(p, cs + (n - 1) * r, r, kLongSlice / VEC, zt, 32, true);
-        if (ce > cs + n * r) zero_rows<NW>(p, cs + n * r, ce - cs - n * r, kLongSlice / VEC, zt, 32);
+        if (two) zero_rows<NW>(p, cs + (n - 1) * r, r, SC / VEC, zt, 32, true);
+        if (ce > cs + n * r) zero_rows<NW>(p, cs + n * r, ce - cs - n * r, SC / VEC, zt, 32);
       }
       const int64_t c_first = sCu[0];
       const int64_t c_last = sCu[p.S];
@@ -278,9 +290,9 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
       const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
       const int64_t h0 = min(q1, c_first);
-      if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, kLongSlice / VEC, zt, 32);
+      if (h0 > q0) zero_rows<NW>(p, q0, h0 - q0, SC / VEC, zt, 32);
       const int64_t t0 = max(q0, c_first), t1 = q1;
-      if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, kLongSlice / VEC, zt, 32);
+      if (t1 > t0) zero_rows<NW>(p, c_last + (t0 - c_first), t1 - t0, SC / VEC, zt, 32);
     }
     // ------------------------------ producer ------------------------------------------
     if (tid == NCT) {
@@ -305,20 +317,19 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         unsigned char* st = stages + static_cast<size_t>(slot) * p.stage_bytes;
         uint64_t* fb = &full[slot + ((lap & 1u) ? p.depth : 0)];
         const int boxes = has_prev ? 2 : 1;
-        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(boxes * r * 128 * 2 +
-                                                        (BWD ? kLongSlice * 2 : 0)));
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(boxes * r * RB * 2 + (BWD ? SC * 2 : 0)));
         if (has_prev) {  // previous block, first-half columns -> tile rows [0, r)
           tma_load_2d(st, &tm_kv, col0, base - r, fb, pol);
           tma_load_2d(st + kTile, &tm_sc, col0, base - r, fb, pol);
         }
         // own block -> tile rows [r, 2r) at coff=2 (second-half columns), [0, r) at coff=1
-        const int yo = two ? r * 128 : 0;
+        const int yo = two ? r * RB : 0;
         const int x = (two ? d : 0) + col0;
         tma_load_2d(st + yo, &tm_kv, x, base, fb, pol);
         tma_load_2d(st + kTile + yo, &tm_sc, x, base, fb, pol);
         if constexpr (BWD)
-          bulk_load_hint(gring + slot * kLongSlice * 2,
-                         p.dout + static_cast<int64_t>(o) * d + col0, kLongSlice * 2, fb, pol);
+          bulk_load_hint(gring + slot * SC * 2, p.dout + static_cast<int64_t>(o) * d + col0, SC * 2,
+                         fb, pol);
       }
       // done: on the normal path the consumers wait for every copy issued here; after a
       // stop the producer waits for them, unless a stopping thread has seen them
@@ -328,9 +339,9 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   }
 
   // ------------------------------ consumers -------------------------------------------
-  const int grp = tid / kThreads;
+  const int grp = tid / GT;
   const int lane = tid & 31;
-  const int wi = (tid % kThreads) >> 5;  // 16-byte chunk of the slice row (8 columns)
+  const int wi = (tid % GT) >> 5;  // 16-byte chunk of the slice row (8 columns)
   const int pg = lane >> 1;              // position lane
   const int ch = lane & 1;               // which 4 columns of the chunk
   const int cl = wi * 8 + ch * 4;        // first column of this thread inside the slice
@@ -387,10 +398,10 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   uint64_t acc[BWD ? PPG : 1][NW];  // backward dAPE sums of this thread's slots (column pairs)
   const int ib = kPS ? grp * PPG : 0;  // this group's first position index (pg + 16 ib)
   // the position split's exchange of the groups' column max and sums (just below the ring)
-  float (*s_xm)[kLongSlice] = reinterpret_cast<float (*)[kLongSlice]>(
-      smem + p.ring_off - (kPS ? 3 * 2 * kLongSlice * 4 : 0));
-  float (*s_xz)[kLongSlice] = s_xm + 2;
-  float (*s_xa)[kLongSlice] = s_xm + 4;
+  float (*s_xm)[SC] =
+      reinterpret_cast<float (*)[SC]>(smem + p.ring_off - (kPS ? 3 * 2 * SC * 4 : 0));
+  float (*s_xz)[SC] = s_xm + 2;
+  float (*s_xa)[SC] = s_xm + 4;
 #pragma unroll
   for (int i = 0; i < (BWD ? PPG : 1); ++i) acc[i][0] = acc[i][1] = 0ull;
   const uint64_t kL2 = f2_pack(kLog2e, kLog2e);
@@ -401,9 +412,9 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
   // halves (with one half of 8 positions the split even depends on the lane).
   constexpr int kStep = (kPk && PPG >= 2 && !(COFF == 2 && PP <= 2)) ? 2 : 1;
 
-  // this thread's tile offset for position pg + 16 i is sw0 + 2048 i: the swizzle depends on
+  // this thread's tile offset for position pg + 16 i is sw0 + kPos i: the swizzle depends on
   // the tile row only through its low three bits, which are those of pg
-  const int sw0 = swz(pg, wi) + ch * 8;
+  const int sw0 = swz<SC>(pg, wi) + ch * 8;
   const int j0 = kPS ? 0 : grp;
   int s = nrows > j0 ? find_segment(sB, p.S, o0 + j0) : 0;
   // stage of row j and its lap (j / depth) % 4, advanced by RSTEP rows per iteration (RSTEP
@@ -437,8 +448,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
     // again instead of keeping x' (and e) in registers.
     auto x_at = [&](const int ii, const int i, const int w, uint64_t (&x)[NW]) {
       uint32_t sw[NW];
-      if constexpr (PP >= 16) lds_words_fresh<NW>(sw, st + kTile + sw0 + i * 2048);
-      else lds_words<NW>(sw, st + kTile + sw0 + i * 2048);
+      if constexpr (PP >= 16) lds_words_fresh<NW>(sw, st + kTile + sw0 + i * kPos);
+      else lds_words<NW>(sw, st + kTile + sw0 + i * kPos);
       uint64_t a2[NW];
       ape_at(ii, w, a2);
 #pragma unroll
@@ -504,8 +515,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       const int w = pg + 16 * i;
       if (two && w < r && !has_prev) continue;
       uint32_t kw[NW];
-      if constexpr (PP >= 16) lds_words_fresh<NW>(kw, st + sw0 + i * 2048);
-      else lds_words<NW>(kw, st + sw0 + i * 2048);
+      if constexpr (PP >= 16) lds_words_fresh<NW>(kw, st + sw0 + i * kPos);
+      else lds_words<NW>(kw, st + sw0 + i * kPos);
       uint64_t x[NW], ec[NW];
       if constexpr (kRecomp) {
         x_at(ii, i, w, x);
@@ -565,7 +576,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
       }
     } else {
       uint32_t gw[NW];
-      lds_words<NW>(gw, gring + slot * kLongSlice * 2 + cl * 2);
+      lds_words<NW>(gw, gring + slot * SC * 2 + cl * 2);
       const uint64_t qg[NW] = {f2_pack(rz[0] * bf16_lo(gw[0]), rz[1] * bf16_hi(gw[0])),
                                f2_pack(rz[2] * bf16_lo(gw[1]), rz[3] * bf16_hi(gw[1]))};
       const uint64_t noc[NW] = {f2_pack(-oc[0], -oc[1]), f2_pack(-oc[2], -oc[3])};
@@ -576,7 +587,7 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
         const bool prev = two && w < r;
         if (prev && !has_prev) continue;
         uint32_t kw[NW];
-        lds_words_fresh<NW>(kw, st + sw0 + i * 2048);
+        lds_words_fresh<NW>(kw, st + sw0 + i * kPos);
         uint64_t ei[NW];
         if constexpr (kRecomp) {
           uint64_t x[NW];
@@ -594,8 +605,8 @@ __global__ void __launch_bounds__(NG * kThreads + (BWD ? 96 : 32), 1)
           acc[ii][q] = c2_add<kPk>(acc[ii][q], t[q]);
         }
         // dKV and dScore replace the kv and score values of this slot in the stage
-        sts_words2(st + sw0 + i * 2048, f2_to_bf2(kk[0]), f2_to_bf2(kk[1]));
-        sts_words2(st + kTile + sw0 + i * 2048, f2_to_bf2(t[0]), f2_to_bf2(t[1]));
+        sts_words2(st + sw0 + i * kPos, f2_to_bf2(kk[0]), f2_to_bf2(kk[1]));
+        sts_words2(st + kTile + sw0 + i * kPos, f2_to_bf2(t[0]), f2_to_bf2(t[1]));
       }
       // (the zeros owned by a segment's last block are written by the zero warp)
     }

@@ -72,11 +72,16 @@ def small_packs():
         "r64c2_d64": ts.make_custom([260, 70, 10], ratio=64, coff=2, d=64, pad_rows=3, seed=25,
                                     score_scale=4.0),
         "r16c1_d64": ts.make_custom([50, 16, 5], ratio=16, coff=1, d=64, pad_rows=0, seed=26),
-        # 256-position windows (ratio 128 x coff 2) on the long-window kernel: first blocks,
-        # short segment, tail, two column slices
+        # 256-position windows (ratio 128 x coff 2, ratio 256 x coff 1) on the long-window
+        # kernel's 32-column slices: first blocks, short segment, tail, 2-4 column slices, a
+        # head dim that is a multiple of 32 but not of 64
         "r128c2_d128": ts.make_custom([400, 256, 127, 300], ratio=128, coff=2, d=128,
                                       pad_rows=3, seed=27, score_scale=4.0),
         "r128c2_d64": ts.make_custom([520, 128], ratio=128, coff=2, d=64, pad_rows=1, seed=28),
+        "r128c2_d96": ts.make_custom([300, 128, 520, 5], ratio=128, coff=2, d=96, pad_rows=2,
+                                     seed=38, score_scale=4.0),
+        "r256c1_d64": ts.make_custom([600, 256, 255, 1030], ratio=256, coff=1, d=64,
+                                     pad_rows=3, seed=39),
         # generic kernel: head dims that are not a multiple of 8 (several column slices,
         # windows up to its 256-position limit)
         "g_d65_r4c2": ts.make_custom([37, 12, 3, 20], ratio=4, coff=2, d=65, pad_rows=3, seed=30),
@@ -94,7 +99,7 @@ def small_packs():
                                       pad_rows=5, seed=36, score_scale=4.0),
         "r2048c1_d8": ts.make_custom([4200, 2047, 2048], ratio=2048, coff=1, d=8, pad_rows=3,
                                      seed=37),
-        "r128c2_split_d32": ts.make_custom([400, 128, 127], ratio=128, coff=2, d=32, pad_rows=3,
+        "r128c2_split_d16": ts.make_custom([400, 128, 127], ratio=128, coff=2, d=16, pad_rows=3,
                                            seed=12),
         "all_short": ts.make_custom([1, 2, 3], ratio=4, coff=2, d=8, pad_rows=2, seed=13),
         "no_segments": ts.make_custom([], ratio=4, coff=2, d=8, pad_rows=5, seed=14),
@@ -185,12 +190,46 @@ def test_bwd_misaligned(cuda_lib, name):
 
 @pytest.mark.parametrize("name", FULL)
 def test_fwd_full(cuda_lib, name):
-    check_fwd(cuda_lib, ts.make_pack(name))
+    check_fwd(cuda_lib, ts.make_pack(name), label="full:" + name)
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_bwd_full(cuda_lib, name):
-    check_bwd(cuda_lib, ts.make_pack(name))
+    check_bwd(cuda_lib, ts.make_pack(name), label="full:" + name)
+
+
+# 256-position windows take 32-column slices while the SMs would get few rows each, and
+# 64-column slices (the position-split backward) otherwise; the rows per SM follow out_rows,
+# so a generous out_rows puts the small packs on the wide slices. Rows past total_comp stay
+# untouched.
+W256_WIDE = ["r128c2_d128", "r128c2_d64", "r256c1_d64"]
+W256_EXTRA_ROWS = 3000
+
+
+@pytest.mark.parametrize("name", W256_WIDE)
+def test_w256_wide_slices(cuda_lib, name):
+    pack = SMALL[name]
+    rows = pack.total_comp + W256_EXTRA_ROWS
+    ref = oracle.fwd_pack(pack, want_f64=True, want_err=True)
+    got, err = H.run_fwd(cuda_lib, pack, out_rows=rows, prefill_bits=H.BF16_NAN)
+    assert err == 0
+    got = got.reshape(rows, pack.d)
+    assert (got[pack.total_comp:] == H.BF16_NAN).all()
+    rep = compare_bf16("out", got[:pack.total_comp], ref["out"], ref["out_f64"], ref["out_err"])
+    log_reports(name + "+wide", rep)
+    assert rep.fail == 0, str(rep)
+    assert rep.clause2 <= max(2, CLAUSE2_CAP["out"] * rep.n), str(rep)
+    refb = oracle.bwd_pack(pack, want_f64=True, want_err=True)
+    dkv, dsc, dape, err = H.run_bwd(cuda_lib, pack, out_rows=rows, prefill_bits=H.BF16_NAN)
+    assert err == 0
+    r1 = compare_bf16("dkv", dkv, refb["dkv"], refb["dkv_f64"], refb["dkv_err"])
+    r2 = compare_bf16("dscore", dsc, refb["dscore"], refb["dscore_f64"], refb["dscore_err"])
+    r3 = compare_dape(dape, refb["dape_f64"], refb["dape_err"])
+    log_reports(name + "+wide", r1, r2, r3)
+    for rep in (r1, r2, r3):
+        assert rep.fail == 0, str(rep)
+    for rep in (r1, r2):
+        assert rep.clause2 <= max(2, CLAUSE2_CAP[rep.name] * rep.n), str(rep)
 
 
 @pytest.mark.parametrize("name", ["tiny", "many_segments", "r4c2_ragged_d16", "no_segments"])

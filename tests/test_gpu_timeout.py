@@ -33,10 +33,10 @@ CASES = {
                  "bwd"),
     "long_fwd": (lambda: ts.make_custom([50, 16, 5], ratio=16, coff=1, d=64, pad_rows=3, seed=61),
                  "fwd"),
-    # 256-position windows: both consumer groups wait on every row and stop together
-    "long256_bwd": (lambda: ts.make_custom([300, 128], ratio=128, coff=2, d=64, pad_rows=1,
+    # 256-position windows (one 32-column slice, so that row 0 lies in the first CTA alone)
+    "long256_bwd": (lambda: ts.make_custom([300, 128], ratio=128, coff=2, d=32, pad_rows=1,
                                            seed=62), "bwd"),
-    "long256_fwd": (lambda: ts.make_custom([300, 128], ratio=128, coff=2, d=64, pad_rows=1,
+    "long256_fwd": (lambda: ts.make_custom([300, 128], ratio=128, coff=2, d=32, pad_rows=1,
                                            seed=62), "fwd"),
 }
 
