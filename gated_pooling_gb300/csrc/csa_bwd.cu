@@ -10,30 +10,9 @@ namespace csa {
 
 PoolKernel bwd_kernel_for(const Plan& pl) {
   if (pl.generic) return pool_generic_kernel<true>;
-  if (pl.longk) {
-    const bool two = pl.coff == 2;
-    switch (pl.pp) {
-      case 1: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_BWD_GROUPS, 2, true, 64>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_BWD_GROUPS, 1, true, 64>);
-      case 2: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_BWD_GROUPS, 2, true, 64>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_BWD_GROUPS, 1, true, 64>);
-      case 4: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_BWD_GROUPS, 2, true, 64>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_BWD_GROUPS, 1, true, 64>);
-      case 8: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_BWD_GROUPS, 2, true, 64>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_BWD_GROUPS, 1, true, 64>);
-      case 16:  // 256-position windows (ratio 128 at coff 2, ratio 256 at coff 1)
-        if (pl.sc == 32)
-          return two ? reinterpret_cast<PoolKernel>(
-                           pool_long_kernel<16, long_groups(true, 256, 32), 2, true, 32>)
-                     : reinterpret_cast<PoolKernel>(
-                           pool_long_kernel<16, long_groups(true, 256, 32), 1, true, 32>);
-        return two ? reinterpret_cast<PoolKernel>(
-                         pool_long_kernel<16, long_groups(true, 256, 64), 2, true, 64>)
-                   : reinterpret_cast<PoolKernel>(
-                         pool_long_kernel<16, long_groups(true, 256, 64), 1, true, 64>);
-      default: return nullptr;
-    }
-  }
+  if (pl.longk)
+    return pl.sc == 32 ? long_kernel_for<true, 32>(pl.pp, pl.coff == 2)
+                       : long_kernel_for<true, 64>(pl.pp, pl.coff == 2);
   if (pl.tma) {
     const int r = pl.pp / pl.coff, coff = pl.coff;
     // one producer warp or all of them (the plan's np)

@@ -10,30 +10,9 @@ namespace csa {
 
 PoolKernel fwd_kernel_for(const Plan& pl) {
   if (pl.generic) return pool_generic_kernel<false>;
-  if (pl.longk) {
-    const bool two = pl.coff == 2;
-    switch (pl.pp) {
-      case 1: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, 2, false, 64>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<1, CSA_LONG_FWD_GROUPS, 1, false, 64>);
-      case 2: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, 2, false, 64>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<2, CSA_LONG_FWD_GROUPS, 1, false, 64>);
-      case 4: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 2, false, 64>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<4, CSA_LONG_FWD_GROUPS, 1, false, 64>);
-      case 8: return two ? reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 2, false, 64>)
-                         : reinterpret_cast<PoolKernel>(pool_long_kernel<8, CSA_LONG_FWD_GROUPS, 1, false, 64>);
-      case 16:  // 256-position windows (ratio 128 at coff 2, ratio 256 at coff 1)
-        if (pl.sc == 32)
-          return two ? reinterpret_cast<PoolKernel>(
-                           pool_long_kernel<16, long_groups(false, 256, 32), 2, false, 32>)
-                     : reinterpret_cast<PoolKernel>(
-                           pool_long_kernel<16, long_groups(false, 256, 32), 1, false, 32>);
-        return two ? reinterpret_cast<PoolKernel>(
-                         pool_long_kernel<16, long_groups(false, 256, 64), 2, false, 64>)
-                   : reinterpret_cast<PoolKernel>(
-                         pool_long_kernel<16, long_groups(false, 256, 64), 1, false, 64>);
-      default: return nullptr;
-    }
-  }
+  if (pl.longk)
+    return pl.sc == 32 ? long_kernel_for<false, 32>(pl.pp, pl.coff == 2)
+                       : long_kernel_for<false, 64>(pl.pp, pl.coff == 2);
   if (pl.ldg) {
     const int r = pl.pp / pl.coff, coff = pl.coff;
     if (r == 1 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 1, 1>;

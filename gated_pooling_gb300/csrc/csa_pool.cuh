@@ -675,19 +675,18 @@ constexpr int kLongSliceCols = 64;  // columns per half in a long-window CTA sli
 #define CSA_LONG_BWD_GROUPS 2
 #endif
 
-// Columns per CTA slice of the long-window kernel: 64, or 32 for a 256-position window
-// whose head dim is not a multiple of 64 or whose 64-column slices would give the SMs fewer
-// than 16 rows each (the pages' 65k-token r128 coff 2 d128 example: 512 rows of 64 KB per
-// slice, 6.7 per SM). Narrower slices give each CTA twice the rows, half as large, so that
-// the pipeline's fill and drain weigh less: that example's step 60.7 -> 53.2 us; with 27
-// rows per SM (d512) the 64-column slices stay 2% faster. (CSA_LONG_W256_SC = 32 or 64
-// forces one width.)
-#ifndef CSA_LONG_W256_SC
-#define CSA_LONG_W256_SC 0
+// Columns per CTA slice of the long-window kernel: 64, or 32 where the head dim is not a
+// multiple of 64 or 64-column slices would give the SMs fewer than 16 rows each (the pages'
+// 65k-token r128 coff 2 d128 example: 512 rows of 64 KB per slice, 6.7 per SM). Narrower
+// slices give each CTA twice the rows, half as large, so that the pipeline's fill and
+// drain weigh less: that example's step 60.7 -> 53.2 us; with 27 rows per SM (d512) the
+// 64-column slices stay 2% faster. (CSA_LONG_SC = 32 or 64 forces one width.)
+#ifndef CSA_LONG_SC
+#define CSA_LONG_SC 0
 #endif
 inline int long_slice_cols(int W, int d, int64_t out_rows, int sms) {
-  if (W < 256) return kLongSliceCols;
-  if (CSA_LONG_W256_SC != 0) return CSA_LONG_W256_SC;
+  (void)W;
+  if (CSA_LONG_SC != 0) return CSA_LONG_SC;
   if (d % 64 != 0) return 32;
   const int64_t rows_per_sm = out_rows * (d / 64) / (sms > 0 ? sms : 1);
   return rows_per_sm < 16 ? 32 : kLongSliceCols;
@@ -727,7 +726,7 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, int sc, size_t sm
                       Plan* out) {
   const int W = coff * r;
   if (!(W == 16 || W == 32 || W == 64 || W == 128 || (CSA_LONG_W256 && W == 256))) return false;
-  if ((sc != 64 && sc != 32) || (sc == 32 && W != 256) || d % sc != 0) return false;
+  if ((sc != 64 && sc != 32) || d % sc != 0) return false;
   Plan pl;
   pl.longk = true;
   pl.coff = coff;

@@ -650,4 +650,24 @@ __global__ void __launch_bounds__(NG * SC * 4 + (BWD ? 96 : 32), 1)
   }
 }
 
+// The long-window kernel for pp positions per lane (W = 16 pp), coff and a slice width, as
+// the plain kernel pointer the launcher takes (its tensor-map arguments are passed by the
+// launch's argument array).
+template <bool BWD, int SC>
+void (*long_kernel_for(int pp, bool two))(PoolParams) {
+  using K = void (*)(PoolParams);
+#define CSA_LONG_PICK(PP)                                                                   \
+  return two ? reinterpret_cast<K>(pool_long_kernel<PP, long_groups(BWD, 16 * PP, SC), 2, BWD, SC>) \
+             : reinterpret_cast<K>(pool_long_kernel<PP, long_groups(BWD, 16 * PP, SC), 1, BWD, SC>)
+  switch (pp) {
+    case 1: CSA_LONG_PICK(1);
+    case 2: CSA_LONG_PICK(2);
+    case 4: CSA_LONG_PICK(4);
+    case 8: CSA_LONG_PICK(8);
+    case 16: CSA_LONG_PICK(16);  // ratio 128 at coff 2, ratio 256 at coff 1
+    default: return nullptr;
+  }
+#undef CSA_LONG_PICK
+}
+
 }  // namespace csa

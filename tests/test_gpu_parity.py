@@ -55,12 +55,13 @@ def small_packs():
         "r8c1_d136": ts.make_custom([40, 17, 8], ratio=8, coff=1, d=136, pad_rows=3, seed=7),
         "r4c2_d264": ts.make_custom([33, 9], ratio=4, coff=2, d=264, pad_rows=2, seed=8),
         "r5c2_split_d16": ts.make_custom([31, 12, 4], ratio=5, coff=2, d=16, pad_rows=1, seed=9),
-        "r16c2_split_d32": ts.make_custom([70, 33, 15], ratio=16, coff=2, d=32, pad_rows=2, seed=10),
+        "r16c2_split_d16": ts.make_custom([70, 33, 15], ratio=16, coff=2, d=16, pad_rows=2, seed=10),
         "r128c1_d64": ts.make_custom([300, 129, 50], ratio=128, coff=1, d=64, pad_rows=7,
                                      seed=11, score_scale=4.0),
-        # tensor-copy kernel for windows of 16..128 positions (d a multiple of 64): every
+        # tensor-copy kernel for windows of 16..128 positions (d a multiple of 32): every
         # positions-per-lane count, both coff, several column slices, tails and short
-        # segments, padding on both sides
+        # segments, padding on both sides; these few rows take the 32-column slices (the
+        # 64-column ones: test_long_wide_slices)
         "r8c2_d128": ts.make_custom([45, 7, 0, 64, 3], ratio=8, coff=2, d=128, pad_rows=5,
                                     seed=20),
         "r16c2_d64": ts.make_custom([90, 15, 49], ratio=16, coff=2, d=64, pad_rows=2, seed=21),
@@ -72,6 +73,11 @@ def small_packs():
         "r64c2_d64": ts.make_custom([260, 70, 10], ratio=64, coff=2, d=64, pad_rows=3, seed=25,
                                     score_scale=4.0),
         "r16c1_d64": ts.make_custom([50, 16, 5], ratio=16, coff=1, d=64, pad_rows=0, seed=26),
+        "r16c2_d32": ts.make_custom([70, 33, 15], ratio=16, coff=2, d=32, pad_rows=2, seed=47),
+        "r16c2_d96": ts.make_custom([90, 33, 17, 64], ratio=16, coff=2, d=96, pad_rows=2,
+                                    seed=45),
+        "r64c1_d160": ts.make_custom([200, 64, 63, 130], ratio=64, coff=1, d=160, pad_rows=1,
+                                     seed=46, score_scale=4.0),
         # 256-position windows (ratio 128 x coff 2, ratio 256 x coff 1) on the long-window
         # kernel's 32-column slices: first blocks, short segment, tail, 2-4 column slices, a
         # head dim that is a multiple of 32 but not of 64
@@ -198,18 +204,19 @@ def test_bwd_full(cuda_lib, name):
     check_bwd(cuda_lib, ts.make_pack(name), label="full:" + name)
 
 
-# 256-position windows take 32-column slices while the SMs would get few rows each, and
-# 64-column slices (the position-split backward) otherwise; the rows per SM follow out_rows,
-# so a generous out_rows puts the small packs on the wide slices. Rows past total_comp stay
-# untouched.
-W256_WIDE = ["r128c2_d128", "r128c2_d64", "r256c1_d64"]
-W256_EXTRA_ROWS = 3000
+# The long-window kernel takes 32-column slices while the SMs would get few rows each, and
+# 64-column slices (for 256-position windows: the position-split backward) otherwise; the
+# rows per SM follow out_rows, so a generous out_rows puts the small packs on the wide
+# slices. Rows past total_comp stay untouched.
+LONG_WIDE = ["r8c2_d128", "r16c2_d64", "r16c1_d64", "r32c1_d192", "r32c2_d64", "r64c1_d128",
+             "r64c2_d64", "r128c1_d64", "r128c2_d128", "r128c2_d64", "r256c1_d64"]
+WIDE_EXTRA_ROWS = 3000
 
 
-@pytest.mark.parametrize("name", W256_WIDE)
-def test_w256_wide_slices(cuda_lib, name):
+@pytest.mark.parametrize("name", LONG_WIDE)
+def test_long_wide_slices(cuda_lib, name):
     pack = SMALL[name]
-    rows = pack.total_comp + W256_EXTRA_ROWS
+    rows = pack.total_comp + WIDE_EXTRA_ROWS
     ref = oracle.fwd_pack(pack, want_f64=True, want_err=True)
     got, err = H.run_fwd(cuda_lib, pack, out_rows=rows, prefill_bits=H.BF16_NAN)
     assert err == 0

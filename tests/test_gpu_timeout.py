@@ -29,11 +29,12 @@ CASES = {
     "stream_bwd": (lambda: ts.make_pack("tiny"), "bwd"),
     "stream_fwd": (lambda: ts.make_custom([12, 8], ratio=4, coff=2, d=512, pad_rows=2, seed=60),
                    "fwd"),
-    "long_bwd": (lambda: ts.make_custom([50, 16, 5], ratio=16, coff=1, d=64, pad_rows=3, seed=61),
+    # (long windows: one 32-column slice, so that row 0 lies in the first CTA alone)
+    "long_bwd": (lambda: ts.make_custom([50, 16, 5], ratio=16, coff=1, d=32, pad_rows=3, seed=61),
                  "bwd"),
-    "long_fwd": (lambda: ts.make_custom([50, 16, 5], ratio=16, coff=1, d=64, pad_rows=3, seed=61),
+    "long_fwd": (lambda: ts.make_custom([50, 16, 5], ratio=16, coff=1, d=32, pad_rows=3, seed=61),
                  "fwd"),
-    # 256-position windows (one 32-column slice, so that row 0 lies in the first CTA alone)
+    # 256-position windows
     "long256_bwd": (lambda: ts.make_custom([300, 128], ratio=128, coff=2, d=32, pad_rows=1,
                                            seed=62), "bwd"),
     "long256_fwd": (lambda: ts.make_custom([300, 128], ratio=128, coff=2, d=32, pad_rows=1,
