@@ -704,9 +704,28 @@ inline int long_slice_cols(int W, int d, int64_t out_rows, int sms) {
 #ifndef CSA_LONG_W256_BWD_GROUPS
 #define CSA_LONG_W256_BWD_GROUPS 2
 #endif
-constexpr int long_groups(bool bwd, int W, int sc) {
-  return W >= 256 ? (sc == 32 ? 2 : (bwd ? CSA_LONG_W256_BWD_GROUPS : CSA_LONG_W256_FWD_GROUPS))
-                  : (bwd ? CSA_LONG_BWD_GROUPS : CSA_LONG_FWD_GROUPS);
+#ifndef CSA_LONG32_FWD_GROUPS
+#define CSA_LONG32_FWD_GROUPS 3  // forward groups of 4 warps on 32-column slices, W < 256
+#endif
+// 256-position windows on 32-column slices: three groups, with ape in shared memory (the
+// forward keeps x' in registers): r128c2 d128 forward 16.6 -> 14.9 us, backward 35.5 ->
+// 32.2 us against two groups (whose forward keeps ape in registers too). At coff 1 the
+// backward's three groups would spill and it keeps two.
+#ifndef CSA_LONG32_W256_FWD_GROUPS
+#define CSA_LONG32_W256_FWD_GROUPS 3
+#endif
+#ifndef CSA_LONG32_W256_BWD_GROUPS
+#define CSA_LONG32_W256_BWD_GROUPS 3
+#endif
+#ifndef CSA_LONG32_BWD_GROUPS
+#define CSA_LONG32_BWD_GROUPS 2  // backward groups of 4 warps on 32-column slices, W < 256
+#endif
+constexpr int long_groups(bool bwd, int W, int sc, int coff) {
+  return W >= 256 ? (sc == 32 ? (bwd ? (coff == 2 ? CSA_LONG32_W256_BWD_GROUPS : 2)
+                                     : CSA_LONG32_W256_FWD_GROUPS)
+                              : (bwd ? CSA_LONG_W256_BWD_GROUPS : CSA_LONG_W256_FWD_GROUPS))
+                  : (bwd ? (sc == 32 ? CSA_LONG32_BWD_GROUPS : CSA_LONG_BWD_GROUPS)
+                         : (sc == 32 ? CSA_LONG32_FWD_GROUPS : CSA_LONG_FWD_GROUPS));
 }
 // The position split: two groups on a 64-column slice of a 256-position window.
 constexpr bool long_position_split(int W, int ng, int sc) {
@@ -740,7 +759,7 @@ inline bool plan_long(bool bwd, int S, int r, int coff, int d, int sc, size_t sm
   pl.slots = 1;
   pl.box_rows = r;
   pl.sB_words = ((S + 1) + 3) & ~3;
-  const int ng = long_groups(bwd, W, sc);
+  const int ng = long_groups(bwd, W, sc, coff);
   const bool ape_smem = !long_ape_in_regs(bwd, W, ng, sc);
   const size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
   // the position split's column max and sums exchange ([3][2 groups][sc columns] floats)

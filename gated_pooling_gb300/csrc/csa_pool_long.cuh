@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(NG * SC * 4 + (BWD ? 96 : 32), 1)
   constexpr int kPos = 16 * RB;   // tile bytes between a lane's positions pg + 16 i
   constexpr int GT = SC * 4;      // threads of a consumer group (SC / 8 warps)
   constexpr int NCT = NG * GT;    // consumer threads
-  static_assert(NG >= 1 && (!BWD || NG <= 2), "the dAPE combine handles two groups");
+  static_assert(NG >= 1 && (!BWD || NG <= 4), "the dAPE combine handles up to four groups");
   // the position split (two groups on a 64-column slice of a 256-position window): both
   // groups take every row, group g the positions [128 g, 128 g + 128) (the previous block,
   // then the own block), and they merge the column max and the sums through shared memory;
@@ -621,21 +621,26 @@ __global__ void __launch_bounds__(NG * SC * 4 + (BWD ? 96 : 32), 1)
   if constexpr (BWD) {
     // the CTA's dAPE partial for this thread's slots: group 0's sums, then group 1's (with
     // the position split each group owns its positions' slots)
-    if constexpr (NG == 2 && !kPS) {
-      asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // ape no longer read
-      if (grp == 1)
+    if constexpr (NG >= 2 && !kPS) {
+      // group h's sums pass through the ape area to group 0, which adds them in group order
+      for (int h = 1; h < NG; ++h) {
+        // ape, or the previous group's sums, no longer read
+        asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
+        if (grp == h)
 #pragma unroll
-        for (int i = 0; i < PP; ++i)
-          sAp[pg + 16 * i] = make_float4(f2_lo(acc[i][0]), f2_hi(acc[i][0]), f2_lo(acc[i][1]),
-                                         f2_hi(acc[i][1]));
-      asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
-      if (grp == 1) return;
+          for (int i = 0; i < PP; ++i)
+            sAp[pg + 16 * i] = make_float4(f2_lo(acc[i][0]), f2_hi(acc[i][0]),
+                                           f2_lo(acc[i][1]), f2_hi(acc[i][1]));
+        asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
+        if (grp == 0)
 #pragma unroll
-      for (int i = 0; i < PP; ++i) {
-        const float4 o1v = sAp[pg + 16 * i];
-        acc[i][0] = c2_add<kPk>(acc[i][0], f2_pack(o1v.x, o1v.y));
-        acc[i][1] = c2_add<kPk>(acc[i][1], f2_pack(o1v.z, o1v.w));
+          for (int i = 0; i < PP; ++i) {
+            const float4 o1v = sAp[pg + 16 * i];
+            acc[i][0] = c2_add<kPk>(acc[i][0], f2_pack(o1v.x, o1v.y));
+            acc[i][1] = c2_add<kPk>(acc[i][1], f2_pack(o1v.z, o1v.w));
+          }
       }
+      if (grp != 0) return;
     }
     float* dst = p.partial + static_cast<int64_t>(g) * r * C;
 #pragma unroll
@@ -657,8 +662,8 @@ template <bool BWD, int SC>
 void (*long_kernel_for(int pp, bool two))(PoolParams) {
   using K = void (*)(PoolParams);
 #define CSA_LONG_PICK(PP)                                                                   \
-  return two ? reinterpret_cast<K>(pool_long_kernel<PP, long_groups(BWD, 16 * PP, SC), 2, BWD, SC>) \
-             : reinterpret_cast<K>(pool_long_kernel<PP, long_groups(BWD, 16 * PP, SC), 1, BWD, SC>)
+  return two ? reinterpret_cast<K>(pool_long_kernel<PP, long_groups(BWD, 16 * PP, SC, 2), 2, BWD, SC>) \
+             : reinterpret_cast<K>(pool_long_kernel<PP, long_groups(BWD, 16 * PP, SC, 1), 1, BWD, SC>)
   switch (pp) {
     case 1: CSA_LONG_PICK(1);
     case 2: CSA_LONG_PICK(2);
