@@ -188,19 +188,7 @@ csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t
       cudaSuccess)
     return CSA_ERR_CUDA;
   if (bps < 1) return CSA_ERR_UNSUPPORTED;  // shared memory of the plan does not fit
-  // row groups: as many as fill the SMs' resident CTAs once over the K column slices,
-  // rounded down (rounding up would leave the last few CTAs to run in a second wave after
-  // the rest, nearly doubling the time when K does not divide that count)
-  int64_t want = static_cast<int64_t>(sms) * bps / pl->K;
-  if (want < 1) want = 1;
-  // the generic kernel's many small CTAs: at most one row group per SM, so that its dAPE
-  // partials need no more workspace than the vector kernels'
-  if (pl->generic && want > sms) want = sms;
-  const int64_t cap = out_rows > 0 ? out_rows : 1;
-  int64_t R = want < cap ? want : cap;
-  if (R < 1) R = 1;
-  if (R > 65535) R = 65535;
-  pl->R = static_cast<int>(R);
+  pl->R = row_groups(*pl, sms, bps, out_rows);
   return CSA_OK;
 }
 

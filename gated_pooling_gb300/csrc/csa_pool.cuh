@@ -477,6 +477,23 @@ struct Plan {
 
 inline int positions_per_thread(int W) { return W >= 5 ? 8 : (W >= 3 ? 4 : W); }
 
+// Row groups R of a plan (grid = K column slices x R): as many as fill the SMs' resident
+// CTAs (sms x bps) once over the K slices, rounded down -- rounding up would leave the last
+// few CTAs to run in a second wave after the rest, nearly doubling the time when K does not
+// divide that count -- at least 1 and at most the row count (and 65535, the grid's y
+// limit). The generic kernel's many small CTAs take at most one row group per SM, so that
+// its dAPE partials need no more workspace than the vector kernels'.
+inline int row_groups(const Plan& pl, int sms, int bps, int64_t out_rows) {
+  int64_t want = static_cast<int64_t>(sms) * bps / (pl.K > 0 ? pl.K : 1);
+  if (want < 1) want = 1;
+  if (pl.generic && want > sms) want = sms;
+  const int64_t cap = out_rows > 0 ? out_rows : 1;
+  int64_t R = want < cap ? want : cap;
+  if (R < 1) R = 1;
+  if (R > 65535) R = 65535;
+  return static_cast<int>(R);
+}
+
 // Geometry that does not depend on the device.
 inline Plan plan_shape(bool bwd, int S, int r, int coff, int d) {
   Plan pl;
