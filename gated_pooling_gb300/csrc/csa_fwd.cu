@@ -15,13 +15,24 @@ PoolKernel fwd_kernel_for(const Plan& pl) {
                        : long_kernel_for<false, 64>(pl.pp, pl.coff == 2);
   if (pl.ldg) {
     const int r = pl.pp / pl.coff, coff = pl.coff;
-    if (r == 1 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 1, 1>;
-    if (r == 2 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 2, 1>;
-    if (r == 4 && coff == 1) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 4, 1>;
-    if (r == 8 && coff == 1) return pool_fwd_ldg_kernel<ldg_threads(8), 8, 1>;
-    if (r == 1 && coff == 2) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 1, 2>;
-    if (r == 2 && coff == 2) return pool_fwd_ldg_kernel<CSA_LDG_THREADS, 2, 2>;
-    if (r == 4 && coff == 2) return pool_fwd_ldg_kernel<ldg_threads(8), 4, 2>;
+#define CSA_LDG_PICK(RR, CC, VV)                                                    \
+  if (r == RR && coff == CC && pl.vec == VV)                                        \
+    return pool_fwd_ldg_kernel<ldg_threads(RR * CC, VV), RR, CC, VV>;
+    CSA_LDG_PICK(1, 1, 4)
+    CSA_LDG_PICK(2, 1, 4)
+    CSA_LDG_PICK(4, 1, 4)
+    CSA_LDG_PICK(8, 1, 4)
+    CSA_LDG_PICK(1, 2, 4)
+    CSA_LDG_PICK(2, 2, 4)
+    CSA_LDG_PICK(4, 2, 4)
+    CSA_LDG_PICK(1, 1, 8)
+    CSA_LDG_PICK(2, 1, 8)
+    CSA_LDG_PICK(1, 2, 8)
+#if CSA_LDG_VEC8_MAX_WINDOW >= 4
+    CSA_LDG_PICK(4, 1, 8)
+    CSA_LDG_PICK(2, 2, 8)
+#endif
+#undef CSA_LDG_PICK
     return nullptr;
   }
   if (pl.tma) {

@@ -5,8 +5,10 @@
 // The forward reads ~95% of its bytes. For short windows and narrow rows the bulk-copy
 // pipeline's per-row and start-up costs dominate (a stage per row of a few KB), so this
 // variant keeps everything in registers: each thread
-// owns one chunk of 4 columns of a row (both halves at coff=2) and loads, per row, the
-// 2*W 8-byte pieces of its window (kv and score) itself. The loads of the thread's next
+// owns one chunk of VEC columns of a row (both halves at coff=2) and loads, per row, the
+// 2*W pieces of its window (kv and score) itself: 16-byte pieces (8 columns) for windows
+// of up to 2 positions, 8-byte pieces (4 columns) for longer windows, whose buffers keep
+// more rows in flight at 8 bytes. The loads of the thread's next
 // PF rows are in flight while a row is computed (a ring of PF + 1 register buffers; PF is
 // larger for shorter windows, whose buffers are smaller), so that enough bytes are in
 // flight to cover the memory latency. CTAs are persistent (one per SM, or two) and own a
@@ -17,16 +19,18 @@
 
 namespace csa {
 
-template <int NT, int R, int COFF>
+template <int NT, int R, int COFF, int VEC>
 __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const PoolParams p) {
-  constexpr int VEC = 4, NW = 2, NH = 1;
+  static_assert(VEC == 4 || VEC == 8, "chunks of 4 or 8 columns");
+  constexpr int NW = VEC / 2;  // 32-bit words (column pairs) per piece
+  constexpr int NQ = VEC / 4;  // ape float4s per chunk
   constexpr int W = R * COFF;
   constexpr bool TWO = COFF == 2;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   int* sB = reinterpret_cast<int*>(smem);
   int* sCu = sB + p.sB_words;
-  float4* sA = reinterpret_cast<float4*>(smem + p.ape_off);  // [W][V] float4, x log2(e)
+  float4* sA = reinterpret_cast<float4*>(smem + p.ape_off);  // [W][V][NQ] float4, x log2(e)
 
   const int TC = build_block_prefix(p.cu, p.S, R, p.capacity, p.out_rows, p.dev_error, sB,
                                     warp_sums, sCu);
@@ -40,12 +44,12 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
   const int o1 = static_cast<int>(static_cast<int64_t>(g + 1) * TC / p.R);
   const int nrows = o1 - o0;
 
-  for (int it = tid; it < W * V; it += NT) {
-    const int w = it / V;
-    const int ch = it % V;
+  for (int it = tid; it < W * V * NQ; it += NT) {
+    const int w = it / (V * NQ);
+    const int ch = (it / NQ) % V;
     const bool prev = TWO && w < R;
     const int arow = (TWO && !prev) ? w - R : w;
-    const int col = ((TWO && !prev) ? d : 0) + ch * VEC;
+    const int col = ((TWO && !prev) ? d : 0) + ch * VEC + (it % NQ) * 4;
     float4 a = __ldg(reinterpret_cast<const float4*>(p.ape + static_cast<int64_t>(arow) * C + col));
     a.x *= kLog2e;
     a.y *= kLog2e;
@@ -86,11 +90,15 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
     }
   };
 
-  // rows in flight ahead of the one being computed
+  // rows in flight ahead of the one being computed (16-byte pieces: one row fewer, for the
+  // same bytes in flight)
 #ifndef CSA_LDG_PF4
 #define CSA_LDG_PF4 2  // rows ahead for windows of 4 positions
 #endif
-  constexpr int PF = W >= 8 ? 1 : (W >= 4 ? CSA_LDG_PF4 : 3);
+#ifndef CSA_LDG_PF4_V8
+#define CSA_LDG_PF4_V8 1  // the same with 16-byte pieces
+#endif
+  constexpr int PF = W >= 8 ? 1 : (W >= 4 ? (VEC == 8 ? CSA_LDG_PF4_V8 : CSA_LDG_PF4) : (VEC == 8 ? 2 : 3));
   uint32_t kv[PF + 1][W][NW], sc[PF + 1][W][NW];
   bool hp[PF + 1];
 #pragma unroll
@@ -111,8 +119,13 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
         for (int q = 0; q < NW; ++q) x[i][q] = f2_pack(-INFINITY, -INFINITY);
         continue;
       }
-      const float4 a = sA[i * V + vl];
-      const uint64_t a2[2] = {f2_pack(a.x, a.y), f2_pack(a.z, a.w)};
+      uint64_t a2[NW];
+#pragma unroll
+      for (int q4 = 0; q4 < NQ; ++q4) {
+        const float4 a = sA[(i * V + vl) * NQ + q4];
+        a2[2 * q4] = f2_pack(a.x, a.y);
+        a2[2 * q4 + 1] = f2_pack(a.z, a.w);
+      }
 #pragma unroll
       for (int q = 0; q < NW; ++q) x[i][q] = f2_fma(bf2_to_f2(scb[i][q]), kL2, a2[q]);
     }
@@ -171,7 +184,6 @@ __global__ void __launch_bounds__(NT, CSA_LDG_CTAS) pool_fwd_ldg_kernel(const Po
       }
     }
   }
-  (void)NH;
 }
 
 }  // namespace csa

@@ -570,7 +570,23 @@ constexpr int stream_producers(bool bwd) {
 #ifndef CSA_LDG_THREADS_W8
 #define CSA_LDG_THREADS_W8 384
 #endif
-constexpr int ldg_threads(int window) { return window >= 8 ? CSA_LDG_THREADS_W8 : CSA_LDG_THREADS; }
+// 16-byte pieces (8 columns a thread, 256 threads a CTA) for windows of up to
+// CSA_LDG_VEC8_MAX_WINDOW positions when d % 8 == 0: windows of 1-2 positions measured
+// 25% faster with them (4x16384 r2 c1 d512 forward 42.7 -> 32.1 us; 35.2 at 384 threads),
+// 4-position windows 3-13% slower (fewer rows or fewer threads in flight, to fit the
+// registers)
+#ifndef CSA_LDG_VEC8_MAX_WINDOW
+#define CSA_LDG_VEC8_MAX_WINDOW 2
+#endif
+#ifndef CSA_LDG_THREADS_V8
+#define CSA_LDG_THREADS_V8 256
+#endif
+constexpr int ldg_vec(int window, int d) {
+  return (window <= CSA_LDG_VEC8_MAX_WINDOW && d % 8 == 0) ? 8 : 4;
+}
+constexpr int ldg_threads(int window, int vec) {
+  return window >= 8 ? CSA_LDG_THREADS_W8 : (vec == 8 ? CSA_LDG_THREADS_V8 : CSA_LDG_THREADS);
+}
 #ifndef CSA_LDG_CTAS
 #define CSA_LDG_CTAS 1
 #endif
@@ -657,11 +673,11 @@ inline bool plan_fwd_ldg(int S, int r, int coff, int d, size_t smem_limit, Plan*
   Plan pl;
   pl.ldg = true;
   pl.coff = coff;
-  pl.vec = 4;
+  pl.vec = ldg_vec(coff * r, d);
   pl.pp = coff * r;
   pl.P = 1;
-  pl.V = d / 4;
-  const int nt = ldg_threads(coff * r);
+  pl.V = d / pl.vec;
+  const int nt = ldg_threads(coff * r, pl.vec);
   if (pl.V > nt) return false;
   pl.Vs = pl.V;
   pl.K = 1;

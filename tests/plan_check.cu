@@ -82,6 +82,19 @@ void check_stream(int bwd, int r, int coff, int d) {
          pl.stage_bytes);
 }
 
+void check_ldg(int r, int coff, int d) {
+  csa::Plan pl;
+  if (!csa::plan_fwd_ldg(3, r, coff, d, kLimit, &pl)) return;
+  const int W = r * coff;
+  expect(pl.vec == 4 || pl.vec == 8, "ldg: chunks of 4 or 8 columns", W, coff, d, 0, pl.vec);
+  if (pl.vec == 8) expect(W <= 4 && d % 8 == 0, "ldg: 16-byte pieces for short windows", W, coff, d, 0);
+  expect(pl.V * pl.vec == d && pl.slots >= 1 && pl.slots * pl.V <= pl.threads,
+         "ldg: a row's chunks fit the block", W, coff, d, 0, pl.slots);
+  expect(pl.smem <= kLimit, "ldg: shared memory within the limit", W, coff, d, 0, (long)pl.smem);
+  expect(pl.threads % 32 == 0 && pl.threads <= 1024, "ldg: block size", W, coff, d, 0,
+         pl.threads);
+}
+
 void check_row_groups() {
   for (int generic = 0; generic < 2; ++generic)
     for (int bps = 1; bps <= 4; ++bps)
@@ -113,6 +126,7 @@ int main() {
         for (int d : dims) {
           for (int64_t rows : {1L, 64L, 512L, 4096L, 100000L}) check_long(bwd, r, coff, d, rows);
           check_stream(bwd, r, coff, d);
+          if (!bwd) check_ldg(r, coff, d);
         }
   // the slice-width rule: 32 columns while 64-column slices give the SMs fewer than 16 rows
   expect(csa::long_slice_cols(256, 128, 512, kSms) == 32, "few rows: 32 columns", 256, 2, 128,
