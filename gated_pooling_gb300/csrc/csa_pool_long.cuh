@@ -1,37 +1,40 @@
 // csa_pool_long.cuh -- pooling kernel for long windows (W = coff*ratio in {16, 32, 64, 128,
 // 256}; e.g. the ratio=128 family of "Megatron-LM PR #5984", commit "add dedicated
 // ratio=128 kernels", at coff 1 and 2), forward and backward, for head dims that are
-// multiples of the slice width (64 columns; 32 for 256-position windows).
+// multiples of the slice width SC.
 //
 // Same operation and zero ownership as pool_kernel (csa_pool.cuh). A CTA owns a slice of SC
-// columns per half (64, or 32 for 256-position windows, whose rows are few: narrower slices
-// give each CTA twice the rows, half as large) and a contiguous range of output rows. For
-// each row a producer warp loads the slice's window with 2-D tensor-map bulk copies (TMA,
-// 2·SC-byte swizzle): one box of [ratio tokens x SC columns] per tensor per block half (at
-// coff=2 the previous block at
-// the slice's first-half columns, the own block at its second-half columns), plus the dout
-// slice in the backward, into a ring of shared-memory stages completing on mbarriers. The
-// backward writes each slot's dKV and dScore over the kv and score values it has consumed in
-// the stage (every slot has exactly one reader and writer), and a store warp copies the
-// finished tiles out with tensor-map bulk stores, whole tile rows at a time, and hands the
-// stage back to the producer as soon as they have been read out. A zero warp writes meanwhile the zeros of short
-// segments, of the rows outside [cu[0], cu[S]), and of the segments whose last block is a
-// row of the CTA (that block's own first-half columns at coff=2, and the segment's tail).
+// columns per half (64, or 32 where the head dim is not a multiple of 64 or the SMs would
+// get few rows each: narrower slices give each CTA twice the rows, half as large;
+// long_slice_cols in csa_pool.cuh) and a contiguous range of output rows. For each row a
+// producer warp loads the slice's window with 2-D tensor-map bulk copies (TMA, 2·SC-byte
+// swizzle): one box of [ratio tokens x SC columns] per tensor per block half (at coff=2
+// the previous block at the slice's first-half columns, the own block at its second-half
+// columns), plus the dout slice in the backward, into a ring of shared-memory stages
+// completing on mbarriers. The backward writes each slot's dKV and dScore over the kv and
+// score values it has consumed in the stage (every slot has exactly one reader and
+// writer), and a store warp copies the finished tiles out with tensor-map bulk stores,
+// whole tile rows at a time, and hands the stage back to the producer as soon as they have
+// been read out. A zero warp writes meanwhile the zeros of short segments, of the rows
+// outside [cu[0], cu[S]), and of the segments whose last block is a row of the CTA (that
+// block's own first-half columns at coff=2, and the segment's tail).
 //
 // Consumers are NG groups of SC/8 warps; group h takes the rows h, h+NG, ... of the CTA's
-// range (more groups keep more warps in flight where registers allow). Warp wi of a
-// group owns the 8 columns [8wi, 8wi+8) of the slice; its lane (pg = lane / 2,
-// ch = lane % 2) owns 4 of them and the window positions pg, pg+16, pg+32, ... A column's
-// max and its sums (sum e, sum e*kv) are reduced over the 16 position lanes with xor
-// shuffles; the adds of a butterfly are commutative, so all 16 lanes end with the same
-// bits and the result is the same on every run. Warps never wait for each other: a stage
-// is released once the threads of its group have arrived on its `empty` barrier. The
-// swizzle puts the 8 rows that each half-warp reads at once on disjoint banks. The ape
-// values of a thread's slots are kept in registers (forward, one group) or in shared
-// memory; in the backward the registers hold the thread's dAPE sums, which the groups add
-// in a fixed order into the CTA's partial at the end. With two backward groups the
-// softmax terms are recomputed from the staged tile in each pass instead of being kept in
-// registers. All waits are bounded.
+// range (more groups keep more warps in flight where registers allow), except in the
+// position split of 256-position windows on 64-column slices, where both groups take every
+// row, each half of its positions. Warp wi of a group owns the 8 columns [8wi, 8wi+8) of
+// the slice; its lane (pg = lane / 2, ch = lane % 2) owns 4 of them and the window
+// positions pg, pg+16, pg+32, ... A column's max and its sums (sum e, sum e*kv) are
+// reduced over the 16 position lanes with xor shuffles; the adds of a butterfly are
+// commutative, so all 16 lanes end with the same bits and the result is the same on every
+// run. Groups never wait for each other (the position split's two groups excepted): a
+// stage is released once the threads of its group have arrived on its `empty` barrier.
+// The swizzle puts the 8 rows that each half-warp reads at once on disjoint banks. The ape
+// values of a thread's slots are kept in registers (forwards of 8 consumer warps, and the
+// position split) or in shared memory; in the backward the registers hold the thread's
+// dAPE sums, which the groups add in a fixed order into the CTA's partial at the end. With
+// several backward groups, or 16 positions per lane, the softmax terms are recomputed from
+// the staged tile in each pass instead of being kept in registers. All waits are bounded.
 #pragma once
 
 #include <cuda.h>
