@@ -761,8 +761,13 @@ constexpr int long_groups(bool bwd, int W, int sc, int coff) {
                          : (sc == 32 ? CSA_LONG32_FWD_GROUPS : CSA_LONG_FWD_GROUPS));
 }
 // The position split: two groups on a 64-column slice of a 256-position window.
+// (the split measured slower for shorter windows, whose lanes then keep the softmax terms
+// in registers: long_r128_d512 backward 56.1 -> 58.3 us, 64-position windows up to +60%)
+#ifndef CSA_LONG_PS_MIN_WINDOW
+#define CSA_LONG_PS_MIN_WINDOW 256
+#endif
 constexpr bool long_position_split(int W, int ng, int sc) {
-  return ng == 2 && W >= 256 && sc == 64;
+  return ng == 2 && W >= CSA_LONG_PS_MIN_WINDOW && sc == 64;
 }
 // The forward keeps a lane's ape in registers where its consumers have 8 warps (registers
 // for 168 a thread) or split the positions; otherwise ape sits in shared memory.

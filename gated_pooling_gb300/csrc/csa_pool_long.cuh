@@ -154,9 +154,10 @@ __global__ void __launch_bounds__(NG * SC * 4 + (BWD ? 96 : 32), 1)
 #endif
   constexpr bool kPk = CSA_LONG_PACKED == 2 || (CSA_LONG_PACKED == 1 && !BWD && PP >= 16);
   // later passes recompute the softmax terms from the staged tile instead of keeping them in
-  // registers: in the backward when two groups share the registers or a lane owns 16
-  // positions, and with the position split (whose forward keeps ape in registers instead)
-  constexpr bool kRecomp = (BWD && (NG > 1 || PP >= 16)) || kPS;
+  // registers: in the backward when several groups share the registers or a lane owns 16
+  // positions, and in the position split when a lane owns 8 (its forward keeps ape in
+  // registers instead)
+  constexpr bool kRecomp = kPS ? PPG >= 8 : (BWD && (NG > 1 || PP >= 16));
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   __shared__ int s_abort;
