@@ -840,9 +840,13 @@ inline bool plan_generic(bool bwd, int S, int r, int coff, int d, size_t smem_li
   pl.K = (d + 127) / 128;
   pl.slots = 1;
   pl.sB_words = ((S + 1) + 3) & ~3;
-  const size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
+  // block prefix, cu_seqlens (cached when it fits: with many segments and a long backward
+  // window the kernel reads it from global memory), then the backward's dAPE sums
+  const size_t sums = bwd ? (size_t)W * 128 * 4 : 0;
+  size_t ape_off = ((size_t)pl.sB_words * 8 + 15) & ~(size_t)15;
+  if (ape_off + sums > smem_limit) ape_off = ((size_t)pl.sB_words * 4 + 15) & ~(size_t)15;
   pl.ape_off = (int)ape_off;
-  pl.smem = ape_off + (bwd ? (size_t)W * 128 * 4 : 0);
+  pl.smem = ape_off + sums;
   if (pl.smem > smem_limit) return false;
   pl.threads = 128;
   *out = pl;

@@ -36,11 +36,16 @@ __global__ void __launch_bounds__(kGenericThreads) pool_generic_kernel(const Poo
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   int* sB = reinterpret_cast<int*>(smem);
+  // cu_seqlens is cached after the block prefix when the plan left room for it (ape_off
+  // past both arrays); with many segments and a long backward window it is read from
+  // global memory instead, so that the dAPE sums fit
+  const bool cu_cached = p.ape_off >= p.sB_words * 8;
   int* sCu = sB + p.sB_words;
   float* acc = reinterpret_cast<float*>(smem + p.ape_off);  // backward: [W][128] dAPE sums
+  auto cu_at = [&](const int s) -> int { return cu_cached ? sCu[s] : __ldg(p.cu + s); };
 
   const int TC = build_block_prefix(p.cu, p.S, p.r, p.capacity, p.out_rows, p.dev_error, sB,
-                                    warp_sums, sCu);
+                                    warp_sums, cu_cached ? sCu : nullptr);
   publish_status(p, TC);
   if (TC < 0) return;
   // (no early launch of the stream's next kernel: it starts when this grid ends, which
@@ -77,12 +82,12 @@ __global__ void __launch_bounds__(kGenericThreads) pool_generic_kernel(const Poo
       const int s_lo = lower_bound_prefix(sB, 0, p.S, o0);
       const int s_hi = (g == p.R - 1) ? p.S : lower_bound_prefix(sB, s_lo, p.S, o1);
       for (int s = s_lo; s < s_hi; ++s) {
-        const int a = sCu[s], b = sCu[s + 1];
+        const int a = cu_at(s), b = cu_at(s + 1);
         if (b - a < r)
           for (int t = a; t < b; ++t) zero_row(t);
       }
-      const int64_t c_first = sCu[0];
-      const int64_t c_last = sCu[p.S];
+      const int64_t c_first = cu_at(0);
+      const int64_t c_last = cu_at(p.S);
       const int64_t npad = c_first + (p.capacity - c_last);
       const int64_t q0 = static_cast<int64_t>(g) * npad / p.R;
       const int64_t q1 = static_cast<int64_t>(g + 1) * npad / p.R;
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(kGenericThreads) pool_generic_kernel(const Poo
       s = advance_segment(sB, s, o);
       const int b = o - sB[s];
       const int n = sB[s + 1] - sB[s];
-      const int base = sCu[s] + b * r;
+      const int base = cu_at(s) + b * r;
       const int w0 = (two && b == 0) ? r : 0;  // first block: no previous half
       auto x_at = [&](int w) {
         const int64_t off = static_cast<int64_t>(tok_of(base, w)) * C + col_of(w);
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(kGenericThreads) pool_generic_kernel(const Poo
               store_bf16_zero(p.dkv + offz);
               store_bf16_zero(p.dscore + offz);
             }
-          for (int t = sCu[s] + n * r; t < sCu[s + 1]; ++t) {
+          for (int t = cu_at(s) + n * r, te = cu_at(s + 1); t < te; ++t) {
             const int64_t offz = static_cast<int64_t>(t) * C + j;
             store_bf16_zero(p.dkv + offz);
             store_bf16_zero(p.dscore + offz);

@@ -95,6 +95,33 @@ void check_ldg(int r, int coff, int d) {
          pl.threads);
 }
 
+// Every shape within the header's limits has a plan: the generic kernel for windows of up
+// to 256 positions at any segment count, the split kernel (plan_shape, always chosen last)
+// within the shared-memory limit for windows of up to 2048.
+void check_envelope() {
+  for (int S : {1, 1000, 16384})
+    for (int bwd = 0; bwd < 2; ++bwd)
+      for (int coff = 1; coff <= 2; ++coff)
+        for (int r = 1; r * coff <= 2048; r *= 2) {
+          const int W = r * coff;
+          for (int d : {8, 13, 64, 512, 4096}) {
+            if (W <= 256) {
+              csa::Plan pg;
+              expect(csa::plan_generic(bwd, S, r, coff, d, kLimit, &pg), "generic plan exists",
+                     W, coff, d, bwd, S);
+              expect(pg.smem <= kLimit && (size_t)pg.ape_off >= (size_t)pg.sB_words * 4,
+                     "generic: block prefix, then the sums, within the limit", W, coff, d, bwd,
+                     S);
+            }
+            if (d % 8 == 0) {
+              const csa::Plan ps = csa::plan_shape(bwd, S, r, coff, d);
+              expect(ps.smem <= kLimit, "split: shared memory within the limit", W, coff, d, bwd,
+                     S);
+            }
+          }
+        }
+}
+
 void check_row_groups() {
   for (int generic = 0; generic < 2; ++generic)
     for (int bps = 1; bps <= 4; ++bps)
@@ -135,6 +162,7 @@ int main() {
          0);
   expect(csa::long_slice_cols(128, 96, 100000, kSms) == 32, "d96: 32 columns", 128, 1, 96, 0);
   check_row_groups();
+  check_envelope();
   if (failures) {
     std::printf("%d of %ld checks failed\n", failures, checks);
     return 1;

@@ -124,6 +124,13 @@ def small_packs():
     packs["max_segments_r16c1_d128"] = ts.make_custom(list(rng.integers(0, 40, 16384)),
                                                       ratio=16, coff=1, d=128, pad_rows=11,
                                                       seed=44)
+    # the generic kernel at the maximum segment count with a 256-position backward window:
+    # the block prefix and the dAPE sums leave no room for cached cu_seqlens, which the
+    # kernel then reads from global memory
+    lens = list(rng.integers(0, 4, 16384))
+    lens[5], lens[700], lens[9000], lens[16383] = 300, 256, 129, 513
+    packs["max_segments_g_r128c2_d13"] = ts.make_custom(lens, ratio=128, coff=2, d=13,
+                                                        pad_rows=5, seed=48)
     lead = ts.make_custom([6, 9, 14], ratio=4, coff=2, d=16, pad_rows=3, seed=17)
     # same tensors with cu_seqlens starting at 6: rows 0..5 become padding, and the one
     # block of the dropped first segment leaves dout
