@@ -57,7 +57,7 @@ PAGE_FWD_BWD_US = {"1x8192_d128": 4.5 + 12.8, "3x8192_d128": 10.0 + 22.2,
 # compressor's backward call, the dAPE partials the reduction kernel reads (row groups x
 # ratio x coff*d x 4 bytes). Re-measured whenever a kernel changes.
 ROOFLINE_TRAFFIC = {"3x8192_d512": 108.2688e6 + 3223553 * 32 + 152 * 4 * 1024 * 4,
-                    "long_r128_d512": 137.371904e6 + 4349953 * 32 + 19 * 128 * 512 * 4,
+                    "long_r128_d512": 137.305344e6 + 4349953 * 32 + 19 * 128 * 512 * 4,
                     "kpool_64x8192_d128_p4": 268.466176e6 + 1048576 * 32}
 
 
