@@ -168,20 +168,10 @@ csa_status_t make_plan(bool bwd, int32_t S, int32_t ratio, int32_t coff, int32_t
   if (note(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
       cudaSuccess)
     return CSA_ERR_CUDA;
-  // Forward windows of <= 8 positions (or narrow rows) take the register-load kernel, other
-  // windows of <= 8 positions the block-streaming kernel, windows of 16..128 positions with
-  // d % 64 == 0 the tensor-copy kernel, everything else the split kernel; shapes or
-  // pointers the vector kernels cannot take go to the generic kernel.
   const size_t limit = static_cast<size_t>(optin) - 256;  // static shared memory headroom
-  if (!fast) {
-    if (!plan_generic(bwd, S, ratio, coff, d, limit, pl)) return CSA_ERR_UNSUPPORTED;
-  } else if (!(!bwd && plan_fwd_ldg(S, ratio, coff, d, limit, pl)) &&
-             !plan_stream(bwd, S, ratio, coff, d, limit, pl) &&
-             !(encode_fn() != nullptr &&
-               plan_long(bwd, S, ratio, coff, d, long_slice_cols(coff * ratio, d, out_rows, sms),
-                         limit, pl))) {
-    *pl = plan_shape(bwd, S, ratio, coff, d);
-  }
+  if (!choose_plan(bwd, S, ratio, coff, d, out_rows, sms, fast, encode_fn() != nullptr, limit,
+                   pl))
+    return CSA_ERR_UNSUPPORTED;
   *kernel = bwd ? bwd_kernel_for(*pl) : fwd_kernel_for(*pl);
   if (*kernel == nullptr) return CSA_ERR_UNSUPPORTED;
   if (blocks_per_sm(dev, reinterpret_cast<const void*>(*kernel), pl->threads, pl->smem, &bps) !=

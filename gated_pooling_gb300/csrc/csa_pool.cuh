@@ -853,4 +853,23 @@ inline bool plan_generic(bool bwd, int S, int r, int coff, int d, size_t smem_li
   return true;
 }
 
+// The plan of a call, in order of preference: forward windows of <= 8 positions (or
+// narrow rows) take the register-load kernel, other windows of <= 8 positions the
+// block-streaming kernel, windows of 16..256 positions the tensor-copy kernel (`tensor_maps`:
+// the driver's tensor-map encoder is available), everything else the split kernel; shapes
+// or pointers the vector kernels cannot take (`fast` false) go to the generic kernel.
+// Returns false for a generic shape that does not fit. make_plan (csa_api.cu) adds the
+// kernel and the row groups.
+inline bool choose_plan(bool bwd, int S, int r, int coff, int d, int64_t out_rows, int sms,
+                        bool fast, bool tensor_maps, size_t smem_limit, Plan* pl) {
+  if (!fast) return plan_generic(bwd, S, r, coff, d, smem_limit, pl);
+  if (!bwd && plan_fwd_ldg(S, r, coff, d, smem_limit, pl)) return true;
+  if (plan_stream(bwd, S, r, coff, d, smem_limit, pl)) return true;
+  if (tensor_maps &&
+      plan_long(bwd, S, r, coff, d, long_slice_cols(coff * r, d, out_rows, sms), smem_limit, pl))
+    return true;
+  *pl = plan_shape(bwd, S, r, coff, d);
+  return true;
+}
+
 }  // namespace csa

@@ -1,11 +1,12 @@
 // Host-side checks of the launch planning (no GPU needed): the geometry the plan functions
 // of csa_pool.cuh produce for a sweep of shapes must fit the device limits and the layout
-// the kernels index, and the row-group rule must never spill CTAs into a second wave.
-// Built with nvcc and run by tests/test_plan.py; prints "ok <checks>" or the failures.
+// the kernels index, every plan the library can choose must have a kernel instantiation,
+// and the row-group rule must never spill CTAs into a second wave. Built with nvcc against
+// the library's objects and run by tests/test_plan.py; prints "ok <checks>" or the failures.
 #include <cstdio>
 #include <cstdlib>
 
-#include "csa_pool.cuh"
+#include "csa_internal.h"
 
 namespace {
 
@@ -122,6 +123,33 @@ void check_envelope() {
         }
 }
 
+// Every shape within the header's limits gets a plan from choose_plan (the library's own
+// choice) and that plan a kernel: a plan without an instantiation would make a valid call
+// return CSA_ERR_UNSUPPORTED.
+void check_dispatch() {
+  for (int fast = 0; fast < 2; ++fast)
+    for (int bwd = 0; bwd < 2; ++bwd)
+      for (int S : {1, 3, 16384})
+        for (int coff = 1; coff <= 2; ++coff)
+          for (int r : {1, 2, 3, 4, 5, 8, 16, 32, 64, 128, 256, 512, 1024, 2048}) {
+            const int W = r * coff;
+            if (W > 2048 || (!fast && W > 256)) continue;
+            for (int d : {8, 13, 16, 24, 32, 64, 96, 128, 160, 192, 264, 512, 1024, 2048}) {
+              if (fast && d % 8 != 0) continue;
+              for (int64_t rows : {1L, 512L, 100000L}) {
+                csa::Plan pl;
+                const bool ok = csa::choose_plan(bwd, S, r, coff, d, rows, kSms, fast != 0, true,
+                                                 kLimit, &pl);
+                expect(ok, "a plan for every shape within the limits", W, coff, d, bwd, S);
+                if (!ok) continue;
+                const csa::PoolKernel k = bwd ? csa::bwd_kernel_for(pl) : csa::fwd_kernel_for(pl);
+                expect(k != nullptr, "a kernel for every plan", W, coff, d, bwd, S);
+                expect(pl.smem <= kLimit, "the chosen plan's shared memory", W, coff, d, bwd, S);
+              }
+            }
+          }
+}
+
 void check_row_groups() {
   for (int generic = 0; generic < 2; ++generic)
     for (int bps = 1; bps <= 4; ++bps)
@@ -163,6 +191,7 @@ int main() {
   expect(csa::long_slice_cols(128, 96, 100000, kSms) == 32, "d96: 32 columns", 128, 1, 96, 0);
   check_row_groups();
   check_envelope();
+  check_dispatch();
   if (failures) {
     std::printf("%d of %ld checks failed\n", failures, checks);
     return 1;
